@@ -1,0 +1,453 @@
+#!/usr/bin/env python
+"""Throughput of rank-major MoE EP dispatch + combine on one GB300.
+
+A step (a "round") is one ep_dispatch then one ep_combine of a whole EP group
+of virtual ranks, on one stream, with the inputs resident in HBM. The
+combine reads the backend combine-input buffers, filled once (untimed) with
+stand-in expert outputs. L2 is flushed (a 256 MB write) before each timed
+step, outside the step's CUDA events; the workloads' per-round traffic is
+also far larger than L2.
+
+Metric: algorithmic bytes per round / round time, in GB/s, and that as a
+fraction of the measured HBM copy bandwidth. Algorithmic bytes per round,
+with N tokens, P routed (token, rank) pairs, payload row H*b bytes, G scale
+columns, K ids, w = 1 when weights are sent:
+  dispatch reads  N*(H*b + 4G + 4K + 4K*w)
+  dispatch writes P*(H*b + 4G + 4K*w) + ep*ep*T*4K   (routed rows + whole id plane)
+  combine         P*2H (reads) + 8N (routing state) + N*2H (writes)
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs an independent replica of the same
+workload on its own GPU (the EP group is simulated inside one GPU, so there
+is nothing to exchange between GPUs); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "dispatch+combine µs/round and routed-payload GB/s as % of GB300 HBM peak"
+FALLBACK_HBM_GBS = 6800.0
+L2_FLUSH_BYTES = 256 << 20
+KERNEL_SRC = os.path.join(ROOT, "combine_topk_ids_dest_gb300", "csrc", "ep_kernels.cu")
+
+
+# ---------------------------------------------------------------------------
+# bookkeeping
+# ---------------------------------------------------------------------------
+def routed_pairs(inp) -> int:
+    """P: number of (token, destination rank) pairs of the workload."""
+    wl = inp.wl
+    ep, E, epr = wl.ep_size, wl.num_experts, wl.num_experts // wl.ep_size
+    active = torch.tensor([(inp.active_rank_mask >> d) & 1 for d in range(ep)], dtype=torch.bool)
+    P = 0
+    for ids in inp.topk_ids:
+        if ids.shape[0] == 0:
+            continue
+        ids = ids.to(torch.int64)
+        ok = (ids >= 0) & (ids < E)
+        owner = torch.where(ok, ids // epr, torch.zeros_like(ids))
+        hit = torch.zeros(ids.shape[0], ep, dtype=torch.bool)
+        hit.scatter_(1, owner, ok)
+        if wl.enable_rank_mask:
+            hit &= active
+        P += int(hit.sum())
+    return P
+
+
+def round_bytes(inp) -> dict:
+    wl = inp.wl
+    N, P = inp.total_tokens, routed_pairs(inp)
+    ep, K, H, T = wl.ep_size, wl.top_k, wl.hidden, wl.tokens_per_rank
+    hb = H * wl.elem_bytes
+    G = wl.scale_cols if inp.scale is not None else 0
+    w = 1 if inp.topk_weights is not None else 0
+    d_read = N * (hb + 4 * G + 4 * K + 4 * K * w)
+    d_write = P * (hb + 4 * G + 4 * K * w) + ep * ep * T * 4 * K
+    c_read = P * 2 * H + 8 * N
+    c_write = N * 2 * H
+    return dict(N=N, P=P, dispatch=d_read + d_write, combine=c_read + c_write,
+                total=d_read + d_write + c_read + c_write, payload=P * (hb + 4 * G) + N * hb,
+                h2d=N * (hb + 4 * G + 4 * K + 4 * K * w), d2h=N * 2 * H)
+
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback 6.8 TB/s (no measured peak available)"
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, when
+    that summary was taken on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    src = hashlib.sha256(open(KERNEL_SRC, "rb").read()).hexdigest()[:16]
+    pat = re.compile(r"^(\S+)\s+workload=(\S+)\s+dram_bytes_per_launch=(\d+)\s+source_sha256=(\S+)")
+    for line in open(path):
+        m = pat.match(line.strip())
+        if m and m.group(1) == kernel and m.group(2) == workload and m.group(4) == src:
+            return int(m.group(3))
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples every 200 ms while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, device):
+        self.proc, self.path = None, None
+        try:
+            uuid = str(torch.cuda.get_device_properties(device).uuid)
+            sel = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        except Exception:
+            sel = str(device.index or 0)
+        self.sel = sel
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            self.fh = os.fdopen(fd, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", self.sel, f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        if getattr(self, "fh", None) is not None:
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not self.path:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons, power = [], [], set(), []
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+                power.append(float(f[3]))
+            except ValueError:
+                continue
+            for name, v in zip(self.NAMES, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm), "power_w_max": max(power) if power else None}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle leg
+# ---------------------------------------------------------------------------
+def _sample_inputs(inp, m: int):
+    """The first min(m, n_s) tokens of every source rank, as a workload with
+    tokens_per_rank m (the oracle's bounded sample of the full workload)."""
+    wl = inp.wl
+    counts = [min(m, n) for n in inp.num_tokens]
+    sub = lambda lst: None if lst is None else [x[:c] for x, c in zip(lst, counts)]
+    swl = wl.replace(capacity=m, runtime_max=None, counts=("fixed",) + tuple(counts))
+    return workloads.EpInputs(wl=swl, num_tokens=counts, hidden=sub(inp.hidden), scale=sub(inp.scale),
+                              topk_ids=sub(inp.topk_ids), topk_weights=sub(inp.topk_weights),
+                              active_rank_mask=inp.active_rank_mask)
+
+
+def _oracle_round(s, eo):
+    import oracle
+    wl = s.wl
+    oracle.dispatch(wl.ep_size, wl.num_experts, wl.top_k, wl.tokens_per_rank, s.num_tokens, s.hidden,
+                    s.topk_ids, scale=s.scale, topk_weights=s.topk_weights,
+                    mask_enabled=wl.enable_rank_mask, active_rank_mask=s.active_rank_mask)
+    oracle.combine(wl.ep_size, wl.num_experts, wl.top_k, wl.hidden, wl.tokens_per_rank, s.num_tokens,
+                   s.topk_ids, eo, mask_enabled=wl.enable_rank_mask, active_rank_mask=s.active_rank_mask)
+
+
+def oracle_sample(inp, seconds: float):
+    """Picks the number of tokens per rank m whose oracle round takes about
+    `seconds`; returns (sample inputs, expert outputs, bytes, description)."""
+    import numpy as np
+    wl = inp.wl
+    T = wl.tokens_per_rank
+
+    def prep(m):
+        s = _sample_inputs(inp, m)
+        rows = torch.arange(wl.ep_size * m)
+        eo = [workloads.expert_output_rows(1, d, rows, wl.hidden).view(torch.int16).numpy().view(np.uint16)
+              for d in range(wl.ep_size)]
+        return s, eo
+
+    m = 1
+    while True:
+        s, eo = prep(m)
+        t0 = time.perf_counter()
+        _oracle_round(s, eo)
+        dt = time.perf_counter() - t0
+        if dt >= seconds / 4 or m >= T:
+            break
+        m = min(T, max(m + 1, int(m * min(8.0, (seconds / 4) / max(dt, 1e-4)))))
+    m = min(T, max(1, int(round(m * seconds / max(dt, 1e-4)))))
+    s, eo = prep(m)
+    b = round_bytes(s)
+    desc = (f"first {m} of {T} tokens per source rank ({s.total_tokens} of {inp.total_tokens} tokens), "
+            f"all {wl.ep_size} ranks, same ids/masks/payload; single-threaded C oracle")
+    return s, eo, b, desc
+
+
+def run_reference(args, rank, world):
+    """The oracle timed as the reference arm (rank 0 only)."""
+    if rank != 0:
+        return
+    wl = workloads.WORKLOADS[args.workload]
+    inp = workloads.make_inputs(wl)
+    full = round_bytes(inp)
+    per_step = max(0.5, args.reference_seconds / max(1, args.steps + args.warmup))
+    s, eo, b, desc = oracle_sample(inp, per_step)
+    for _ in range(args.warmup):
+        _oracle_round(s, eo)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        _oracle_round(s, eo)
+        times.append(time.perf_counter() - t0)
+    tot = sum(times)
+    gbs = b["total"] * len(times) / tot / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / len(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp32",
+        "data": "synthetic", "config": workload_config(wl, full),
+        "us_per_round_extrapolated": 1e6 * full["total"] / (gbs * 1e9),
+        "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": desc,
+                         "host_cores_available": len(os.sched_getaffinity(0))},
+        "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(wl, b):
+    return {"workload": wl.name, "ep_size": wl.ep_size, "num_experts": wl.num_experts,
+            "top_k": wl.top_k, "hidden": wl.hidden,
+            "payload": wl.dtype + (f" + fp32 scales [n,{wl.scale_cols}]" if wl.scales else ""),
+            "max_tokens_per_rank": wl.capacity, "tokens_per_rank": wl.tokens_per_rank,
+            "ids": wl.ids, "rank_mask_drops": list(wl.dropped_ranks) if wl.dropped_ranks else None,
+            "tokens": b["N"], "routed_pairs": b["P"], "bytes_per_round": b["total"],
+            "l2": "inputs larger than L2 and L2 flushed (256 MB write) before each timed step, "
+                  "outside its events",
+            "combine_input": "backend buffer, filled once with stand-in expert outputs (untimed)"}
+
+
+# ---------------------------------------------------------------------------
+# GPU leg
+# ---------------------------------------------------------------------------
+def run_ours(args, rank, world):
+    import torch.distributed as dist
+    from combine_topk_ids_dest_gb300 import EpComm
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    wl = workloads.WORKLOADS[args.workload]
+    inp = workloads.make_inputs(wl)
+    b = round_bytes(inp)
+    dtype = torch.bfloat16 if wl.dtype == "bf16" else torch.float8_e4m3fn
+    comm = EpComm(wl.ep_size, wl.num_experts, wl.top_k, wl.hidden, wl.capacity, dtype=dtype,
+                  enable_rank_mask=wl.enable_rank_mask, device=dev)
+    mask = inp.active_rank_mask if wl.enable_rank_mask else None
+    hid = [x.to(dev) for x in inp.hidden]
+    ids = [x.to(dev) for x in inp.topk_ids]
+    wts = None if inp.topk_weights is None else [x.to(dev) for x in inp.topk_weights]
+    scl = None if inp.scale is None else [x.to(dev) for x in inp.scale]
+    out = [torch.empty(n, wl.hidden, dtype=torch.bfloat16, device=dev) for n in inp.num_tokens]
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def dispatch():
+        return comm.dispatch(hid, ids, wts, hidden_states_scale=scl,
+                             runtime_max_tokens_per_rank=wl.runtime_max, active_rank_mask=mask)
+
+    def combine():
+        comm.combine(output=out, active_rank_mask=mask)
+
+    # one untimed round to fill the combine-input buffers with expert outputs
+    res = dispatch()
+    rows = torch.arange(wl.ep_size * res.tokens_per_rank, device=dev)
+    for d, buf in enumerate(comm.get_combine_input_buffer()):
+        buf.copy_(workloads.expert_output_rows(1, d, rows, wl.hidden, device=dev))
+    del rows
+    combine()
+    launches_per_round = 2 if wl.ep_size * wl.tokens_per_rank > 0 else 0
+
+    for i in range(args.warmup):
+        flush.fill_(i & 0xFF)
+        dispatch()
+        combine()
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    with ClockSampler(dev) as clocks:
+        torch.cuda.synchronize(dev)
+        for i in range(args.steps):
+            flush.fill_((i + 1) & 0xFF)
+            ev[i][0].record()
+            dispatch()
+            ev[i][1].record()
+            combine()
+            ev[i][2].record()
+        torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    t_disp = [e[0].elapsed_time(e[1]) for e in ev]
+    t_comb = [e[1].elapsed_time(e[2]) for e in ev]
+    t_round = [e[0].elapsed_time(e[2]) for e in ev]
+    total_ms = sum(t_round)
+
+    # end to end through the public API from pinned host memory
+    pin = lambda lst: None if lst is None else [x.pin_memory() for x in lst]
+    h_hid, h_ids, h_w, h_s = pin(inp.hidden), pin(inp.topk_ids), pin(inp.topk_weights), pin(inp.scale)
+    h_out = [torch.empty(n, wl.hidden, dtype=torch.bfloat16).pin_memory() for n in inp.num_tokens]
+    e2e_steps = max(1, min(args.steps, 20))
+
+    def e2e_round():
+        for src, dst in ((h_hid, hid), (h_ids, ids), (h_w, wts), (h_s, scl)):
+            if src is not None:
+                for a, d_ in zip(src, dst):
+                    d_.copy_(a, non_blocking=True)
+        dispatch()
+        combine()
+        for o, h in zip(out, h_out):
+            h.copy_(o, non_blocking=True)
+
+    for _ in range(2):
+        e2e_round()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(e2e_steps):
+        e2e_round()
+    e1.record()
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+
+    if world > 1:
+        t = torch.tensor([total_ms, e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms, e2e_ms = float(t[0]), float(t[1])
+    comm.destroy()
+    if rank != 0:
+        return
+
+    peak, peak_src = hbm_peak()
+    ms = total_ms / args.steps
+    gbs = world * b["total"] * args.steps / (total_ms / 1e3) / 1e9
+    disp_ms, comb_ms = statistics.mean(t_disp), statistics.mean(t_comb)
+    kernels = {
+        "dispatch_kernel": {"bytes": b["dispatch"], "ms": disp_ms},
+        "combine_kernel": {"bytes": b["combine"], "ms": comb_ms},
+    }
+    top = max(kernels, key=lambda k: kernels[k]["ms"])
+    per = {k: {"achieved": v["bytes"] / (v["ms"] / 1e3) / 1e9, "ms": v["ms"], "bytes": v["bytes"],
+               "frac": v["bytes"] / (v["ms"] / 1e3) / 1e9 / peak, "share": v["ms"] / (disp_ms + comb_ms),
+               "traffic": recorded_traffic(k, wl.name)} for k, v in kernels.items()}
+    line = {
+        "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "fp32", "data": "synthetic",
+        "config": workload_config(wl, b),
+        "us_per_round": 1e3 * ms, "us_per_round_median": 1e3 * statistics.median(t_round),
+        "pct_hbm_peak": 100.0 * b["total"] / (ms / 1e3) / 1e9 / peak,
+        "payload_gbs": b["payload"] / (ms / 1e3) / 1e9,
+        "roofline": {"bound": "hbm", "kernel": top, "achieved": per[top]["achieved"], "peak": peak,
+                     "unit": "GB/s", "frac": per[top]["frac"], "traffic": per[top]["traffic"],
+                     "peak_source": peak_src, "kernels": per},
+        "e2e": {"value": world * b["total"] / (e2e_ms / 1e3) / 1e9, "unit": "GB/s", "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": b["h2d"], "d2h_bytes_per_step": b["d2h"], "steps": e2e_steps,
+                "path": "pinned host inputs -> H2D -> EpComm.dispatch/combine (C ABI) -> D2H outputs"},
+        "gpu_launches": launches_per_round * args.steps,
+        "clocks": clocks.summary(),
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        s, eo, sb, desc = oracle_sample(inp, args.cpu_seconds)
+        t0 = time.perf_counter()
+        _oracle_round(s, eo)
+        dt = time.perf_counter() - t0
+        cpu_gbs = sb["total"] / dt / 1e9
+        line["cpu_baseline"] = {"value": cpu_gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                                "sample": desc, "seconds": dt,
+                                "us_per_round_extrapolated": 1e6 * b["total"] / (cpu_gbs * 1e9),
+                                "host_cores_available": len(os.sched_getaffinity(0))}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="dsv3_prefill", choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle sample size, in seconds")
+    ap.add_argument("--reference-seconds", type=float, default=120.0,
+                    help="total oracle time of the reference arm")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        dist.init_process_group("nccl")
+    try:
+        run_ours(args, rank, world)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

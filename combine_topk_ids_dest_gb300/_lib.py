@@ -1,0 +1,106 @@
+"""ctypes declarations of the C ABI in include/ep.h (libep_gb300.so).
+
+Loading fails loudly: there is no fallback implementation of any operation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import build as _build
+
+EP_OK = 0
+EP_ERR_INVALID_ARG = 1
+EP_ERR_STATE = 2
+EP_ERR_CUDA = 3
+EP_ERR_OOM = 4
+EP_ERR_UNSUPPORTED = 5
+STATUS_NAMES = {0: "EP_OK", 1: "EP_ERR_INVALID_ARG", 2: "EP_ERR_STATE", 3: "EP_ERR_CUDA",
+                4: "EP_ERR_OOM", 5: "EP_ERR_UNSUPPORTED"}
+
+EP_DTYPE_BF16 = 0
+EP_DTYPE_FP8_E4M3 = 1
+EP_INVALID_EXPERT_ID = -1
+EP_MAX_EP_SIZE = 64
+EP_MAX_TOP_K = 32
+EP_SCALE_GROUP = 128
+ALL_RANKS = (1 << 64) - 1  # "no mask": every rank active
+
+# Every symbol include/ep.h declares.
+EXPORTS = ("ep_is_supported", "ep_workspace_size", "ep_create", "ep_create_with_workspace",
+           "ep_dispatch", "ep_get_combine_input_buffer", "ep_combine", "ep_destroy",
+           "ep_rank_mask", "ep_last_error")
+
+
+class EpDispatchResultC(ctypes.Structure):
+    _fields_ = [("tokens_per_rank", ctypes.c_int),
+                ("ep_size", ctypes.c_int),
+                ("recv_hidden", ctypes.POINTER(ctypes.c_void_p)),
+                ("recv_scale", ctypes.POINTER(ctypes.c_void_p)),
+                ("recv_topk_ids", ctypes.POINTER(ctypes.c_void_p)),
+                ("recv_topk_weights", ctypes.POINTER(ctypes.c_void_p))]
+
+
+class EpError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = True) -> ctypes.CDLL:
+    """Load libep_gb300.so (building it first if it is missing or stale)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.LIB
+        if build_if_missing:
+            path = _build.build()
+        if not os.path.exists(path):
+            raise ImportError(f"CUDA library {path} is missing; run "
+                              "`python -m combine_topk_ids_dest_gb300.build`")
+        L = ctypes.CDLL(path)
+        P, i32, u64, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint64, ctypes.c_size_t
+        PP = ctypes.POINTER(ctypes.c_void_p)
+        L.ep_is_supported.argtypes = []
+        L.ep_is_supported.restype = i32
+        L.ep_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, ctypes.POINTER(sz)]
+        L.ep_workspace_size.restype = i32
+        L.ep_create.argtypes = [i32, i32, i32, i32, i32, i32, i32, PP]
+        L.ep_create.restype = i32
+        L.ep_create_with_workspace.argtypes = [i32, i32, i32, i32, i32, i32, i32, P, sz, PP]
+        L.ep_create_with_workspace.restype = i32
+        L.ep_dispatch.argtypes = [P, P, P, P, P, P, i32, u64, P, ctypes.POINTER(EpDispatchResultC)]
+        L.ep_dispatch.restype = i32
+        L.ep_get_combine_input_buffer.argtypes = [P, i32, PP]
+        L.ep_get_combine_input_buffer.restype = i32
+        L.ep_combine.argtypes = [P, P, P, u64, P]
+        L.ep_combine.restype = i32
+        L.ep_destroy.argtypes = [P]
+        L.ep_destroy.restype = i32
+        L.ep_rank_mask.argtypes = [ctypes.POINTER(ctypes.c_int), i32]
+        L.ep_rank_mask.restype = u64
+        L.ep_last_error.argtypes = []
+        L.ep_last_error.restype = ctypes.c_char_p
+        _lib = L
+        return L
+
+
+def check(status: int) -> None:
+    if status != EP_OK:
+        msg = load().ep_last_error()
+        raise EpError(status, msg.decode() if msg else "")
+
+
+def ptr_array(ptrs) -> ctypes.Array:
+    """Host array of device pointers (None/0 entries become NULL)."""
+    return (ctypes.c_void_p * len(ptrs))(*[(int(p) if p else None) for p in ptrs])

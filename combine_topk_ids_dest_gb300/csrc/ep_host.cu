@@ -1,0 +1,477 @@
+// ep_host.cu -- the C ABI of include/ep.h: handle, workspace layout, argument
+// and state checks, kernel launches.
+//
+// Contract followed (FlashInfer moe_ep pages):
+//  - "flashinfer.moe_ep.MoEEpCommunication", class description: one
+//    in-flight dispatch/combine pair per instance; every dispatch() is
+//    followed by exactly one combine(). dispatch(): runtime_max_tokens_per_rank
+//    is at most max_tokens_per_rank and sets tokens_per_rank (capacity when
+//    absent). get_combine_input_buffer(): valid only between dispatch() and
+//    combine(). destroy(): idempotent.
+//  - "flashinfer.moe_ep.NVLinkOneSidedAlltoAll", dispatch(): active_rank_mask
+//    requires enable_rank_mask; every rank passes topk_weights or none does
+//    (an empty rank passes an empty tensor). combine(): active_rank_mask must
+//    match the dispatch's. get_combine_input_buffer(): an [ep_size *
+//    tokens_per_rank, hidden_size] view of the rank's combine input region.
+//
+// Workspace (one device allocation, regions 256-byte aligned, each sized at
+// capacity C = max_tokens_per_rank):
+//   recv_hidden  [ep][ep*C][row_bytes]
+//   recv_scale   [ep][ep*C][H/128] fp32     (when H % 128 == 0)
+//   recv_ids     [ep][ep*C][K] int32
+//   recv_weights [ep][ep*C][K] fp32
+//   combine_in   [ep][ep*C][H] bf16
+//   route_mask   [ep*C] uint64
+// A step with tokens_per_rank T uses the first ep*T rows of each region, so
+// receive row s*T+t of rank d sits at region base + d*stride + (s*T+t)*row.
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+
+#include "ep_internal.h"
+
+struct ep_handle {
+    int ep, num_experts, top_k, hidden, capacity, experts_per_rank;
+    ep_dtype dtype;
+    int elem_bytes, row_bytes, scale_cols;
+    int mask_enabled;
+    int device;
+
+    uint8_t *ws;
+    size_t ws_bytes;
+    bool owns_ws;
+    size_t off_hidden, off_scale, off_ids, off_weights, off_comb, off_mask;
+    size_t st_hidden, st_scale, st_ids, st_weights, st_comb;  // bytes per rank region
+
+    // state of the pending dispatch
+    bool pending;
+    int T;
+    uint64_t mask;
+    int32_t counts[EP_MAX_EP_SIZE];
+
+    void *r_hidden[EP_MAX_EP_SIZE];
+    float *r_scale[EP_MAX_EP_SIZE];
+    int32_t *r_ids[EP_MAX_EP_SIZE];
+    float *r_weights[EP_MAX_EP_SIZE];
+};
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+ep_status fail(ep_status st, const char *fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+ep_status ok()
+{
+    g_err[0] = '\0';
+    return EP_OK;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+uint64_t full_mask(int ep) { return ep >= 64 ? ~0ULL : ((1ULL << ep) - 1); }
+
+struct Layout {
+    int elem_bytes, row_bytes, scale_cols;
+    size_t off_hidden, off_scale, off_ids, off_weights, off_comb, off_mask, total;
+    size_t st_hidden, st_scale, st_ids, st_weights, st_comb;
+};
+
+ep_status plan(int ep, int E, int K, int H, int C, ep_dtype dtype, Layout *L)
+{
+    if (ep < 1 || ep > EP_MAX_EP_SIZE)
+        return fail(EP_ERR_INVALID_ARG, "ep_size=%d outside [1, %d]", ep, EP_MAX_EP_SIZE);
+    if (E < ep || E % ep != 0)
+        return fail(EP_ERR_INVALID_ARG, "num_experts=%d is not a positive multiple of ep_size=%d", E, ep);
+    if (K < 1 || K > EP_MAX_TOP_K)
+        return fail(EP_ERR_INVALID_ARG, "top_k=%d outside [1, %d]", K, EP_MAX_TOP_K);
+    if (dtype != EP_DTYPE_BF16 && dtype != EP_DTYPE_FP8_E4M3)
+        return fail(EP_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
+    const int elem = dtype == EP_DTYPE_BF16 ? 2 : 1;
+    if (H < 1 || ((long long)H * elem) % 16 != 0)
+        return fail(EP_ERR_INVALID_ARG, "hidden=%d: a row must be a positive multiple of 16 bytes", H);
+    if (H % 8 != 0)
+        return fail(EP_ERR_INVALID_ARG, "hidden=%d: the bf16 combine rows need hidden %% 8 == 0", H);
+    if (C < 0)
+        return fail(EP_ERR_INVALID_ARG, "max_tokens_per_rank=%d < 0", C);
+    L->elem_bytes = elem;
+    L->row_bytes = H * elem;
+    L->scale_cols = (H % EP_SCALE_GROUP == 0) ? H / EP_SCALE_GROUP : 0;
+    const size_t rows = (size_t)ep * (size_t)C;
+    L->st_hidden = align256(rows * L->row_bytes);
+    L->st_scale = align256(rows * L->scale_cols * sizeof(float));
+    L->st_ids = align256(rows * K * sizeof(int32_t));
+    L->st_weights = align256(rows * K * sizeof(float));
+    L->st_comb = align256(rows * H * 2);
+    size_t off = 0;
+    L->off_hidden = off;
+    off += L->st_hidden * ep;
+    L->off_scale = off;
+    off += L->st_scale * ep;
+    L->off_ids = off;
+    off += L->st_ids * ep;
+    L->off_weights = off;
+    off += L->st_weights * ep;
+    L->off_comb = off;
+    off += L->st_comb * ep;
+    L->off_mask = off;
+    off += align256(rows * sizeof(uint64_t));
+    L->total = off < 256 ? 256 : off;
+    return EP_OK;
+}
+
+ep_status make_handle(int ep, int E, int K, int H, int C, ep_dtype dtype, int enable_rank_mask,
+                      void *ws, size_t ws_bytes, bool own, ep_handle **out)
+{
+    if (!out)
+        return fail(EP_ERR_INVALID_ARG, "out is NULL");
+    *out = nullptr;
+    Layout L;
+    ep_status st = plan(ep, E, K, H, C, dtype, &L);
+    if (st != EP_OK)
+        return st;
+    int dev = 0;
+    cudaError_t ce = cudaGetDevice(&dev);
+    if (ce != cudaSuccess)
+        return fail(EP_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(ce));
+    if (!ep_is_supported())
+        return fail(EP_ERR_UNSUPPORTED, "device %d is not compute capability 10.3 (sm_103)", dev);
+    if (own) {
+        void *p = nullptr;
+        ce = cudaMalloc(&p, L.total);
+        if (ce != cudaSuccess) {
+            cudaGetLastError();
+            return fail(ce == cudaErrorMemoryAllocation ? EP_ERR_OOM : EP_ERR_CUDA,
+                        "cudaMalloc(%zu): %s", L.total, cudaGetErrorString(ce));
+        }
+        ws = p;
+        ws_bytes = L.total;
+    } else {
+        if (!ws || !aligned(ws, 256))
+            return fail(EP_ERR_INVALID_ARG, "workspace is NULL or not 256-byte aligned");
+        if (ws_bytes < L.total)
+            return fail(EP_ERR_INVALID_ARG, "workspace has %zu bytes, needs %zu", ws_bytes, L.total);
+    }
+    ep_handle *h = new (std::nothrow) ep_handle();
+    if (!h) {
+        if (own)
+            cudaFree(ws);
+        return fail(EP_ERR_OOM, "host allocation of the handle failed");
+    }
+    h->ep = ep;
+    h->num_experts = E;
+    h->top_k = K;
+    h->hidden = H;
+    h->capacity = C;
+    h->experts_per_rank = E / ep;
+    h->dtype = dtype;
+    h->elem_bytes = L.elem_bytes;
+    h->row_bytes = L.row_bytes;
+    h->scale_cols = L.scale_cols;
+    h->mask_enabled = enable_rank_mask ? 1 : 0;
+    h->device = dev;
+    h->ws = static_cast<uint8_t *>(ws);
+    h->ws_bytes = ws_bytes;
+    h->owns_ws = own;
+    h->off_hidden = L.off_hidden;
+    h->off_scale = L.off_scale;
+    h->off_ids = L.off_ids;
+    h->off_weights = L.off_weights;
+    h->off_comb = L.off_comb;
+    h->off_mask = L.off_mask;
+    h->st_hidden = L.st_hidden;
+    h->st_scale = L.st_scale;
+    h->st_ids = L.st_ids;
+    h->st_weights = L.st_weights;
+    h->st_comb = L.st_comb;
+    h->pending = false;
+    h->T = 0;
+    h->mask = 0;
+    for (int d = 0; d < ep; ++d) {
+        h->r_hidden[d] = h->ws + h->off_hidden + d * h->st_hidden;
+        h->r_scale[d] = reinterpret_cast<float *>(h->ws + h->off_scale + d * h->st_scale);
+        h->r_ids[d] = reinterpret_cast<int32_t *>(h->ws + h->off_ids + d * h->st_ids);
+        h->r_weights[d] = reinterpret_cast<float *>(h->ws + h->off_weights + d * h->st_weights);
+    }
+    *out = h;
+    return ok();
+}
+
+ep_status check_device(const ep_handle *h)
+{
+    int dev = -1;
+    cudaError_t ce = cudaGetDevice(&dev);
+    if (ce != cudaSuccess)
+        return fail(EP_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(ce));
+    if (dev != h->device)
+        return fail(EP_ERR_INVALID_ARG, "handle lives on device %d but device %d is current", h->device,
+                    dev);
+    return EP_OK;
+}
+
+// Normalises a caller's mask: UINT64_MAX means "all ranks". With masking
+// disabled only "all ranks" is accepted.
+ep_status resolve_mask(const ep_handle *h, uint64_t in, uint64_t *out)
+{
+    const uint64_t full = full_mask(h->ep);
+    if (in == ~0ULL)
+        in = full;
+    if (!h->mask_enabled) {
+        if (in != full)
+            return fail(EP_ERR_INVALID_ARG,
+                        "active_rank_mask 0x%llx given but the handle was created without "
+                        "enable_rank_mask",
+                        (unsigned long long)in);
+    } else if (in & ~full) {
+        return fail(EP_ERR_INVALID_ARG, "active_rank_mask 0x%llx has bits at or above ep_size=%d",
+                    (unsigned long long)in, h->ep);
+    }
+    *out = in;
+    return EP_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int ep_is_supported(void)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return (major == 10 && minor == 3) ? 1 : 0;
+}
+
+ep_status ep_workspace_size(int ep_size, int num_experts, int top_k, int hidden,
+                            int max_tokens_per_rank, ep_dtype dtype, size_t *bytes)
+{
+    if (!bytes)
+        return fail(EP_ERR_INVALID_ARG, "bytes is NULL");
+    Layout L;
+    ep_status st = plan(ep_size, num_experts, top_k, hidden, max_tokens_per_rank, dtype, &L);
+    if (st != EP_OK)
+        return st;
+    *bytes = L.total;
+    return ok();
+}
+
+ep_status ep_create(int ep_size, int num_experts, int top_k, int hidden, int max_tokens_per_rank,
+                    ep_dtype dtype, int enable_rank_mask, ep_handle **out)
+{
+    return make_handle(ep_size, num_experts, top_k, hidden, max_tokens_per_rank, dtype,
+                       enable_rank_mask, nullptr, 0, true, out);
+}
+
+ep_status ep_create_with_workspace(int ep_size, int num_experts, int top_k, int hidden,
+                                   int max_tokens_per_rank, ep_dtype dtype, int enable_rank_mask,
+                                   void *workspace, size_t bytes, ep_handle **out)
+{
+    return make_handle(ep_size, num_experts, top_k, hidden, max_tokens_per_rank, dtype,
+                       enable_rank_mask, workspace, bytes, false, out);
+}
+
+ep_status ep_dispatch(ep_handle *h, const void *const *hidden, const float *const *hidden_scale,
+                      const int32_t *const *topk_ids, const float *const *topk_weights,
+                      const int32_t *num_tokens, int runtime_max_tokens_per_rank,
+                      uint64_t active_rank_mask, void *stream, ep_dispatch_result *out)
+{
+    if (!h)
+        return fail(EP_ERR_INVALID_ARG, "handle is NULL");
+    if (h->pending)
+        return fail(EP_ERR_STATE, "dispatch called while the previous dispatch has not been combined");
+    if (!hidden || !topk_ids || !num_tokens)
+        return fail(EP_ERR_INVALID_ARG, "hidden, topk_ids and num_tokens must not be NULL");
+    ep_status st = check_device(h);
+    if (st != EP_OK)
+        return st;
+    const int T = runtime_max_tokens_per_rank < 0 ? h->capacity : runtime_max_tokens_per_rank;
+    if (T > h->capacity)
+        return fail(EP_ERR_INVALID_ARG, "runtime_max_tokens_per_rank=%d exceeds max_tokens_per_rank=%d",
+                    T, h->capacity);
+    uint64_t mask = 0;
+    st = resolve_mask(h, active_rank_mask, &mask);
+    if (st != EP_OK)
+        return st;
+    if (hidden_scale && h->scale_cols == 0)
+        return fail(EP_ERR_INVALID_ARG, "hidden_scale needs hidden %% %d == 0 (hidden=%d)",
+                    EP_SCALE_GROUP, h->hidden);
+
+    epk::DispatchArgs a;
+    std::memset(&a, 0, sizeof a);
+    for (int s = 0; s < h->ep; ++s) {
+        const int n = num_tokens[s];
+        if (n < 0 || n > T)
+            return fail(EP_ERR_INVALID_ARG, "num_tokens[%d]=%d outside [0, tokens_per_rank=%d]", s, n, T);
+        a.num_tokens[s] = n;
+        if (n == 0)
+            continue;
+        if (!hidden[s] || !aligned(hidden[s], 16))
+            return fail(EP_ERR_INVALID_ARG, "hidden[%d] is NULL or not 16-byte aligned", s);
+        if (!topk_ids[s] || !aligned(topk_ids[s], 4))
+            return fail(EP_ERR_INVALID_ARG, "topk_ids[%d] is NULL or not 4-byte aligned", s);
+        if (hidden_scale && (!hidden_scale[s] || !aligned(hidden_scale[s], 4)))
+            return fail(EP_ERR_INVALID_ARG,
+                        "hidden_scale[%d] is NULL while other ranks pass scales (all or none)", s);
+        if (topk_weights && (!topk_weights[s] || !aligned(topk_weights[s], 4)))
+            return fail(EP_ERR_INVALID_ARG,
+                        "topk_weights[%d] is NULL while other ranks pass weights (all or none)", s);
+        a.hidden[s] = static_cast<const uint8_t *>(hidden[s]);
+        a.ids[s] = topk_ids[s];
+        a.scale[s] = hidden_scale ? hidden_scale[s] : nullptr;
+        a.weights[s] = topk_weights ? topk_weights[s] : nullptr;
+    }
+    a.recv_hidden = h->ws + h->off_hidden;
+    a.hidden_stride = (long long)h->st_hidden;
+    a.recv_scale = reinterpret_cast<float *>(h->ws + h->off_scale);
+    a.scale_stride = (long long)(h->st_scale / sizeof(float));
+    a.recv_ids = reinterpret_cast<int32_t *>(h->ws + h->off_ids);
+    a.ids_stride = (long long)(h->st_ids / sizeof(int32_t));
+    a.recv_weights = reinterpret_cast<float *>(h->ws + h->off_weights);
+    a.weights_stride = (long long)(h->st_weights / sizeof(float));
+    a.route_mask = reinterpret_cast<uint64_t *>(h->ws + h->off_mask);
+    a.active = mask;
+    a.ep = h->ep;
+    a.num_experts = h->num_experts;
+    a.experts_per_rank = h->experts_per_rank;
+    a.top_k = h->top_k;
+    a.T = T;
+    a.row_bytes = h->row_bytes;
+    a.G = hidden_scale ? h->scale_cols : 0;
+    a.has_weights = topk_weights ? 1 : 0;
+
+    cudaError_t ce = epk::launch_dispatch(a, static_cast<cudaStream_t>(stream));
+    if (ce != cudaSuccess)
+        return fail(EP_ERR_CUDA, "dispatch launch: %s", cudaGetErrorString(ce));
+
+    h->pending = true;
+    h->T = T;
+    h->mask = mask;
+    for (int s = 0; s < h->ep; ++s)
+        h->counts[s] = a.num_tokens[s];
+    if (out) {
+        out->tokens_per_rank = T;
+        out->ep_size = h->ep;
+        out->recv_hidden = h->r_hidden;
+        out->recv_scale = hidden_scale ? h->r_scale : nullptr;
+        out->recv_topk_ids = h->r_ids;
+        out->recv_topk_weights = topk_weights ? h->r_weights : nullptr;
+    }
+    return ok();
+}
+
+ep_status ep_get_combine_input_buffer(ep_handle *h, int rank, void **out)
+{
+    if (!h || !out)
+        return fail(EP_ERR_INVALID_ARG, "handle or out is NULL");
+    *out = nullptr;
+    if (!h->pending)
+        return fail(EP_ERR_STATE, "the combine input buffer is valid only between dispatch and combine");
+    if (rank < 0 || rank >= h->ep)
+        return fail(EP_ERR_INVALID_ARG, "rank=%d outside [0, %d)", rank, h->ep);
+    *out = h->ws + h->off_comb + (size_t)rank * h->st_comb;
+    return ok();
+}
+
+ep_status ep_combine(ep_handle *h, const void *const *expert_output, void *const *output,
+                     uint64_t active_rank_mask, void *stream)
+{
+    if (!h)
+        return fail(EP_ERR_INVALID_ARG, "handle is NULL");
+    if (!h->pending)
+        return fail(EP_ERR_STATE, "combine called without a pending dispatch");
+    if (!output)
+        return fail(EP_ERR_INVALID_ARG, "output is NULL");
+    ep_status st = check_device(h);
+    if (st != EP_OK)
+        return st;
+    uint64_t mask = 0;
+    st = resolve_mask(h, active_rank_mask, &mask);
+    if (st != EP_OK)
+        return st;
+    if (mask != h->mask)
+        return fail(EP_ERR_INVALID_ARG, "combine active_rank_mask 0x%llx differs from dispatch's 0x%llx",
+                    (unsigned long long)mask, (unsigned long long)h->mask);
+
+    epk::CombineArgs a;
+    std::memset(&a, 0, sizeof a);
+    for (int d = 0; d < h->ep; ++d) {
+        const void *p = expert_output ? expert_output[d] : nullptr;
+        if (!p)
+            p = h->ws + h->off_comb + (size_t)d * h->st_comb;
+        else if (!aligned(p, 16))
+            return fail(EP_ERR_INVALID_ARG, "expert_output[%d] is not 16-byte aligned", d);
+        a.eo[d] = static_cast<const uint16_t *>(p);
+    }
+    for (int s = 0; s < h->ep; ++s) {
+        a.num_tokens[s] = h->counts[s];
+        if (h->counts[s] == 0)
+            continue;
+        if (!output[s] || !aligned(output[s], 16))
+            return fail(EP_ERR_INVALID_ARG, "output[%d] is NULL or not 16-byte aligned", s);
+        a.out[s] = static_cast<uint16_t *>(output[s]);
+    }
+    a.route_mask = reinterpret_cast<const uint64_t *>(h->ws + h->off_mask);
+    a.ep = h->ep;
+    a.T = h->T;
+    a.H = h->hidden;
+
+    cudaError_t ce = epk::launch_combine(a, static_cast<cudaStream_t>(stream));
+    if (ce != cudaSuccess)
+        return fail(EP_ERR_CUDA, "combine launch: %s", cudaGetErrorString(ce));
+    h->pending = false;
+    return ok();
+}
+
+ep_status ep_destroy(ep_handle *h)
+{
+    if (!h)
+        return ok();
+    ep_status st = EP_OK;
+    if (h->owns_ws && h->ws) {
+        int prev = -1;
+        cudaGetDevice(&prev);
+        if (prev != h->device)
+            cudaSetDevice(h->device);
+        cudaError_t ce = cudaFree(h->ws);
+        if (prev >= 0 && prev != h->device)
+            cudaSetDevice(prev);
+        if (ce != cudaSuccess)
+            st = fail(EP_ERR_CUDA, "cudaFree: %s", cudaGetErrorString(ce));
+    }
+    delete h;
+    return st == EP_OK ? ok() : st;
+}
+
+uint64_t ep_rank_mask(const int *ranks, int n)
+{
+    uint64_t m = 0;
+    if (!ranks)
+        return 0;
+    for (int i = 0; i < n; ++i)
+        if (ranks[i] >= 0 && ranks[i] < 64)
+            m |= 1ULL << ranks[i];
+    return m;
+}
+
+const char *ep_last_error(void) { return g_err; }
+
+}  // extern "C"

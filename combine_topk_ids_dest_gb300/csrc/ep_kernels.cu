@@ -1,0 +1,283 @@
+// ep_kernels.cu -- sm_103a kernels of rank-major MoE EP dispatch/combine with
+// every EP rank a virtual rank in this GPU's memory.
+//
+// dispatch_kernel (one warp per source slot s*T+t, grid-stride):
+//   routing   -- lane k reads expert id k; the owners' bits are OR-reduced
+//                across the warp (two 32-bit halves for up to 64 ranks) and
+//                ANDed with active_rank_mask ("flashinfer.moe_ep.
+//                NVLinkOneSidedAlltoAll", dispatch(): tokens routed to a
+//                masked-off rank are dropped). The bit set is kept for combine.
+//   id plane  -- the slot's id row in every destination rank: the token's ids
+//                where it is routed, invalid_expert_id elsewhere and on padding
+//                slots (same page, class description).
+//   payload   -- the hidden row is read once with 16-byte non-caching loads
+//                and stored to every routed rank's row s*T+t, followed by the
+//                scale and weight rows ("hidden_states, its optional scale
+//                factors, topk_ids and topk_weights travel as payloads of a
+//                single dispatch").
+//
+// combine_kernel (one thread per 16-byte column vector of one output row):
+//   reads the row's slot in each routed rank's combine input in ascending
+//   rank order (loads of up to 8 ranks in flight before their adds), adds in
+//   fp32 from +0.0 and rounds once to bf16 ("flashinfer.moe_ep.
+//   MoEEpCommunication", combine(): each token's expert outputs, summed over
+//   ranks).
+//
+// Nothing here is a dense contraction; both kernels are bound by HBM
+// bandwidth, so the design is about coalesced 16-byte accesses and enough
+// bytes in flight per SM.
+#include "ep_internal.h"
+
+namespace epk {
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+constexpr int kDispatchThreads = 256;  // 8 warps, one slot each
+constexpr int kDispatchVecPerLane = 8;  // 16-byte vectors per lane per chunk (4 KB per warp)
+constexpr int kCombineThreads = 128;
+constexpr int kCombineBatch = 8;  // rank rows loaded before their adds
+
+__device__ __forceinline__ uint4 ld_stream(const void *p)
+{
+    uint4 v;
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+        : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// Two fp32 -> packed bf16x2, round to nearest even (cvt.rn.bf16x2.f32; no
+// flush of subnormals). `lo` lands in the low half.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+{
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+__global__ void __launch_bounds__(kDispatchThreads)
+    dispatch_kernel(const __grid_constant__ DispatchArgs a)
+{
+    const int lane = threadIdx.x & 31;
+    const int wpb = blockDim.x >> 5;
+    const long long n_slots = (long long)a.ep * a.T;
+    const long long warp_stride = (long long)gridDim.x * wpb;
+    const int K = a.top_k;
+
+    for (long long slot = (long long)blockIdx.x * wpb + (threadIdx.x >> 5); slot < n_slots;
+         slot += warp_stride) {
+        const int s = (int)(slot / a.T);
+        const int t = (int)(slot - (long long)s * a.T);
+        const bool live = t < a.num_tokens[s];
+
+        // ---- routing: destination-rank bit set of this slot
+        int my_id = EP_INVALID_EXPERT_ID;
+        unsigned lo = 0, hi = 0;
+        if (live && lane < K) {
+            my_id = a.ids[s][(long long)t * K + lane];
+            if (my_id >= 0 && my_id < a.num_experts) {
+                const int owner = my_id / a.experts_per_rank;
+                if (owner < 32)
+                    lo = 1u << owner;
+                else
+                    hi = 1u << (owner - 32);
+            }
+        }
+        lo = __reduce_or_sync(kFull, lo);
+        hi = __reduce_or_sync(kFull, hi);
+        const uint64_t m = ((((uint64_t)hi) << 32) | lo) & a.active;
+        if (lane == 0)
+            a.route_mask[slot] = m;
+
+        // ---- id rows of this slot in all destination ranks
+        int32_t *ids_slot = a.recv_ids + slot * K;
+        if ((K & 3) == 0) {
+            const int qpr = K >> 2;  // int4 vectors per id row
+            const int n = a.ep * qpr;
+            for (int base = 0; base < n; base += 32) {
+                const int i = base + lane;
+                const int d = i / qpr;
+                const int q = i - d * qpr;
+                int4 v;
+                v.x = __shfl_sync(kFull, my_id, 4 * q + 0);
+                v.y = __shfl_sync(kFull, my_id, 4 * q + 1);
+                v.z = __shfl_sync(kFull, my_id, 4 * q + 2);
+                v.w = __shfl_sync(kFull, my_id, 4 * q + 3);
+                if (i < n) {
+                    if (!((m >> d) & 1u))
+                        v = make_int4(EP_INVALID_EXPERT_ID, EP_INVALID_EXPERT_ID,
+                                      EP_INVALID_EXPERT_ID, EP_INVALID_EXPERT_ID);
+                    *reinterpret_cast<int4 *>(ids_slot + d * a.ids_stride + 4 * q) = v;
+                }
+            }
+        } else {
+            const int n = a.ep * K;
+            for (int base = 0; base < n; base += 32) {
+                const int i = base + lane;
+                const int d = i / K;
+                const int k = i - d * K;
+                int v = __shfl_sync(kFull, my_id, k);
+                if (i < n) {
+                    if (!((m >> d) & 1u))
+                        v = EP_INVALID_EXPERT_ID;
+                    ids_slot[d * a.ids_stride + k] = v;
+                }
+            }
+        }
+        if (m == 0)
+            continue;  // warp-uniform: padding, unrouted or fully masked slot
+
+        // ---- hidden row: read once, store to each routed rank
+        const int nvec = a.row_bytes >> 4;
+        const uint8_t *src = a.hidden[s] + (long long)t * a.row_bytes;
+        uint8_t *dst_slot = a.recv_hidden + slot * a.row_bytes;
+        for (int c0 = 0; c0 < nvec; c0 += 32 * kDispatchVecPerLane) {
+            uint4 v[kDispatchVecPerLane];
+#pragma unroll
+            for (int j = 0; j < kDispatchVecPerLane; ++j) {
+                const int idx = c0 + j * 32 + lane;
+                if (idx < nvec)
+                    v[j] = ld_stream(src + 16 * (long long)idx);
+            }
+            for (uint64_t mm = m; mm; mm &= mm - 1) {
+                const int d = __ffsll((long long)mm) - 1;
+                uint4 *dst = reinterpret_cast<uint4 *>(dst_slot + d * a.hidden_stride);
+#pragma unroll
+                for (int j = 0; j < kDispatchVecPerLane; ++j) {
+                    const int idx = c0 + j * 32 + lane;
+                    if (idx < nvec)
+                        dst[idx] = v[j];
+                }
+            }
+        }
+
+        // ---- scale row (G fp32) and weight row (K fp32)
+        if (a.G > 0) {
+            const float *ssrc = a.scale[s] + (long long)t * a.G;
+            float *sdst = a.recv_scale + slot * a.G;
+            for (int j = lane; j < a.G; j += 32) {
+                const float x = ssrc[j];
+                for (uint64_t mm = m; mm; mm &= mm - 1) {
+                    const int d = __ffsll((long long)mm) - 1;
+                    sdst[d * a.scale_stride + j] = x;
+                }
+            }
+        }
+        if (a.has_weights && lane < K) {
+            const float w = a.weights[s][(long long)t * K + lane];
+            float *wdst = a.recv_weights + slot * K + lane;
+            for (uint64_t mm = m; mm; mm &= mm - 1) {
+                const int d = __ffsll((long long)mm) - 1;
+                wdst[d * a.weights_stride] = w;
+            }
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kCombineThreads)
+    combine_kernel(const __grid_constant__ CombineArgs a, int blocks_per_row, long long n_blocks)
+{
+    const int nvec = a.H >> 3;  // 8 bf16 per 16-byte vector
+    for (long long b = blockIdx.x; b < n_blocks; b += gridDim.x) {
+        const long long slot = b / blocks_per_row;
+        const int chunk = (int)(b - slot * blocks_per_row);
+        const int s = (int)(slot / a.T);
+        const int t = (int)(slot - (long long)s * a.T);
+        if (t >= a.num_tokens[s])
+            continue;  // block-uniform
+        const int v = chunk * kCombineThreads + threadIdx.x;
+        if (v >= nvec)
+            continue;
+        const uint64_t m = a.route_mask[slot];
+        const long long off = (slot * a.H) * 2 + 16 * (long long)v;  // byte offset in a rank's buffer
+
+        float acc[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            acc[e] = 0.0f;
+
+        uint64_t mm = m;
+        while (mm) {
+            uint4 x[kCombineBatch];
+            int nb = 0;
+#pragma unroll
+            for (int j = 0; j < kCombineBatch; ++j) {
+                if (mm) {
+                    const int d = __ffsll((long long)mm) - 1;
+                    mm &= mm - 1;
+                    x[j] = ld_stream(reinterpret_cast<const uint8_t *>(a.eo[d]) + off);
+                    nb = j + 1;
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < kCombineBatch; ++j) {
+                if (j < nb) {
+                    acc[0] = __fadd_rn(acc[0], bf16_lo(x[j].x));
+                    acc[1] = __fadd_rn(acc[1], bf16_hi(x[j].x));
+                    acc[2] = __fadd_rn(acc[2], bf16_lo(x[j].y));
+                    acc[3] = __fadd_rn(acc[3], bf16_hi(x[j].y));
+                    acc[4] = __fadd_rn(acc[4], bf16_lo(x[j].z));
+                    acc[5] = __fadd_rn(acc[5], bf16_hi(x[j].z));
+                    acc[6] = __fadd_rn(acc[6], bf16_lo(x[j].w));
+                    acc[7] = __fadd_rn(acc[7], bf16_hi(x[j].w));
+                }
+            }
+        }
+        uint4 o;
+        o.x = pack_bf16x2(acc[0], acc[1]);
+        o.y = pack_bf16x2(acc[2], acc[3]);
+        o.z = pack_bf16x2(acc[4], acc[5]);
+        o.w = pack_bf16x2(acc[6], acc[7]);
+        reinterpret_cast<uint4 *>(a.out[s] + (long long)t * a.H)[v] = o;
+    }
+}
+
+int sm_count()
+{
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return 152;
+    if (!cached[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            n = 152;
+        cached[dev] = n;
+    }
+    return cached[dev];
+}
+
+}  // namespace
+
+cudaError_t launch_dispatch(const DispatchArgs &a, cudaStream_t stream)
+{
+    const long long n_slots = (long long)a.ep * a.T;
+    if (n_slots == 0)
+        return cudaSuccess;
+    const int wpb = kDispatchThreads / 32;
+    long long blocks = (n_slots + wpb - 1) / wpb;
+    const long long cap = (long long)sm_count() * 8;  // 8 resident blocks of 256 per SM
+    if (blocks > cap)
+        blocks = cap;
+    dispatch_kernel<<<(unsigned)blocks, kDispatchThreads, 0, stream>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const CombineArgs &a, cudaStream_t stream)
+{
+    const int nvec = a.H >> 3;
+    const int bpr = (nvec + kCombineThreads - 1) / kCombineThreads;
+    const long long n_blocks = (long long)a.ep * a.T * bpr;
+    if (n_blocks == 0)
+        return cudaSuccess;
+    long long grid = n_blocks;
+    if (grid > (1LL << 30))
+        grid = 1LL << 30;
+    combine_kernel<<<(unsigned)grid, kCombineThreads, 0, stream>>>(a, bpr, n_blocks);
+    return cudaGetLastError();
+}
+
+}  // namespace epk

@@ -1,0 +1,262 @@
+"""PyTorch binding of the C ABI (include/ep.h): argument marshalling only.
+
+Mirrors FlashInfer's ``MoEEpCommunication`` / ``NVLinkOneSidedAlltoAll``
+interface (pages "flashinfer.moe_ep.MoEEpCommunication" and
+"flashinfer.moe_ep.NVLinkOneSidedAlltoAll": ``is_platform_supported``,
+``dispatch``, ``combine``, ``get_combine_input_buffer``, ``active_rank_mask``,
+``destroy``) for an EP group whose ``ep_size`` ranks are virtual ranks on one
+GPU. Every per-rank argument is a list with one tensor per rank; every
+result is a list with one tensor per rank. All work runs in the CUDA library
+on torch's current stream; torch supplies device memory and streams only.
+"""
+from __future__ import annotations
+
+import ctypes
+from dataclasses import dataclass
+from typing import List, Optional, Sequence
+
+import torch
+
+from . import _lib
+from ._lib import ALL_RANKS, EpError, check, ptr_array
+
+_DTYPES = {torch.bfloat16: _lib.EP_DTYPE_BF16, torch.float8_e4m3fn: _lib.EP_DTYPE_FP8_E4M3}
+
+
+@dataclass
+class EpDispatchResult:
+    """Receive buffers of every rank after one dispatch (MoEEpDispatchResult).
+
+    ``hidden_states[d]`` is rank d's ``[ep_size*tokens_per_rank, hidden]``
+    receive buffer; row ``s*tokens_per_rank + t`` is token t of source rank s.
+    Rows of tokens not routed to d, and padding rows, carry ``topk_ids`` of
+    all -1; only their id rows are defined. The tensors view the handle's
+    workspace: valid until destroy(), overwritten by the next dispatch().
+    """
+
+    tokens_per_rank: int
+    hidden_states: List[torch.Tensor]
+    hidden_states_scale: Optional[List[torch.Tensor]]
+    topk_ids: List[torch.Tensor]
+    topk_weights: Optional[List[torch.Tensor]]
+
+
+def _mask_value(m) -> int:
+    if m is None:
+        return ALL_RANKS
+    if isinstance(m, torch.Tensor):
+        if m.numel() != 1:
+            raise ValueError("active_rank_mask must hold one uint64")
+        return int(m.reshape(-1)[0].item()) & ALL_RANKS
+    return int(m) & ALL_RANKS
+
+
+def _stream_ptr(device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+class EpComm:
+    """Rank-major MoE EP dispatch/combine over ``ep_size`` virtual ranks.
+
+    ``dtype`` is the hidden payload type: ``torch.bfloat16`` or
+    ``torch.float8_e4m3fn`` (fp8 rows usually travel with fp32 per-128-column
+    scales). The workspace is allocated here with torch, at capacity
+    ``max_tokens_per_rank``.
+    """
+
+    def __init__(self, ep_size: int, num_experts: int, top_k: int, hidden: int,
+                 max_tokens_per_rank: int, dtype: torch.dtype = torch.bfloat16,
+                 enable_rank_mask: bool = False, device=None):
+        self._L = _lib.load()
+        if dtype not in _DTYPES:
+            raise ValueError(f"dtype {dtype} not supported (bfloat16 or float8_e4m3fn)")
+        self.ep_size, self.num_experts, self.top_k = int(ep_size), int(num_experts), int(top_k)
+        self.hidden, self.max_tokens_per_rank = int(hidden), int(max_tokens_per_rank)
+        self.dtype, self.enable_rank_mask = dtype, bool(enable_rank_mask)
+        self.device = torch.device("cuda", torch.cuda.current_device()) if device is None \
+            else torch.device(device)
+        self._h = None
+        nbytes = ctypes.c_size_t(0)
+        check(self._L.ep_workspace_size(self.ep_size, self.num_experts, self.top_k, self.hidden,
+                                        self.max_tokens_per_rank, _DTYPES[dtype],
+                                        ctypes.byref(nbytes)))
+        with torch.cuda.device(self.device):
+            self._ws = torch.empty(nbytes.value, dtype=torch.uint8, device=self.device)
+            h = ctypes.c_void_p()
+            check(self._L.ep_create_with_workspace(
+                self.ep_size, self.num_experts, self.top_k, self.hidden, self.max_tokens_per_rank,
+                _DTYPES[dtype], int(self.enable_rank_mask), ctypes.c_void_p(self._ws.data_ptr()),
+                nbytes.value, ctypes.byref(h)))
+        self._h = h
+        self._counts: Optional[List[int]] = None
+        self._T = 0
+
+    # -- MoEEpCommunication.is_platform_supported ---------------------------
+    @classmethod
+    def is_platform_supported(cls) -> bool:
+        if not torch.cuda.is_available():
+            return False
+        return bool(_lib.load().ep_is_supported())
+
+    # -- NVLinkOneSidedAlltoAll.active_rank_mask ----------------------------
+    @staticmethod
+    def active_rank_mask(active_ranks: Sequence[int]) -> torch.Tensor:
+        """CPU uint64 bit mask of ``active_ranks``."""
+        arr = (ctypes.c_int * len(active_ranks))(*[int(r) for r in active_ranks])
+        m = _lib.load().ep_rank_mask(arr, len(active_ranks))
+        return torch.tensor([m], dtype=torch.uint64)
+
+    def _view(self, ptr: int, rows: int, cols: int, dtype: torch.dtype) -> torch.Tensor:
+        off = int(ptr) - self._ws.data_ptr()
+        nbytes = rows * cols * torch.empty((), dtype=dtype).element_size()
+        return self._ws[off:off + nbytes].view(dtype).view(rows, cols)
+
+    def _live(self):
+        if self._h is None:
+            raise EpError(_lib.EP_ERR_STATE, "the communicator was destroyed")
+
+    def _check_rank_tensor(self, name, t, s, n, cols, dtype):
+        if t.device != self.device:
+            raise ValueError(f"{name}[{s}] is on {t.device}, expected {self.device}")
+        if t.dtype != dtype:
+            raise ValueError(f"{name}[{s}] has dtype {t.dtype}, expected {dtype}")
+        if t.dim() != 2 or t.shape[0] != n or t.shape[1] != cols or not t.is_contiguous():
+            raise ValueError(f"{name}[{s}] must be a contiguous [{n}, {cols}] tensor, got "
+                             f"{tuple(t.shape)}")
+
+    # -- MoEEpCommunication.dispatch ----------------------------------------
+    def dispatch(self, hidden_states: Sequence[torch.Tensor], topk_ids: Sequence[torch.Tensor],
+                 topk_weights: Optional[Sequence[torch.Tensor]] = None, *,
+                 hidden_states_scale: Optional[Sequence[torch.Tensor]] = None,
+                 runtime_max_tokens_per_rank: Optional[int] = None,
+                 eplb_local_stats: Optional[Sequence[torch.Tensor]] = None,
+                 active_rank_mask=None) -> EpDispatchResult:
+        """Send every rank's tokens to the ranks that own their experts.
+
+        Per rank s: ``hidden_states[s]`` [n_s, hidden] (dtype of the
+        communicator), ``topk_ids[s]`` int32 [n_s, top_k], optional
+        ``topk_weights[s]`` fp32 [n_s, top_k] and ``hidden_states_scale[s]``
+        fp32 [n_s, hidden/128]. Weights and scales are all-or-none over ranks.
+        """
+        self._live()
+        if eplb_local_stats is not None:
+            raise NotImplementedError("eplb_local_stats is not supported by this backend")
+        ep, K, H = self.ep_size, self.top_k, self.hidden
+        if len(hidden_states) != ep or len(topk_ids) != ep:
+            raise ValueError(f"hidden_states and topk_ids need {ep} per-rank tensors")
+        for name, lst in (("topk_weights", topk_weights), ("hidden_states_scale", hidden_states_scale)):
+            if lst is not None and (len(lst) != ep or any(x is None for x in lst)):
+                raise ValueError(f"{name}: every rank passes it or none does "
+                                 "(an empty rank passes an empty tensor)")
+        counts = [int(x.shape[0]) for x in hidden_states]
+        G = H // _lib.EP_SCALE_GROUP
+        for s in range(ep):
+            n = counts[s]
+            self._check_rank_tensor("hidden_states", hidden_states[s], s, n, H, self.dtype)
+            self._check_rank_tensor("topk_ids", topk_ids[s], s, n, K, torch.int32)
+            if topk_weights is not None:
+                self._check_rank_tensor("topk_weights", topk_weights[s], s, n, K, torch.float32)
+            if hidden_states_scale is not None:
+                self._check_rank_tensor("hidden_states_scale", hidden_states_scale[s], s, n, G,
+                                        torch.float32)
+        c_counts = (ctypes.c_int32 * ep)(*counts)
+        res = _lib.EpDispatchResultC()
+        rt = -1 if runtime_max_tokens_per_rank is None else int(runtime_max_tokens_per_rank)
+        if rt < -1:
+            raise ValueError("runtime_max_tokens_per_rank must be >= 0")
+        with torch.cuda.device(self.device):
+            check(self._L.ep_dispatch(
+                self._h, ptr_array([x.data_ptr() for x in hidden_states]),
+                ptr_array([x.data_ptr() for x in hidden_states_scale]) if hidden_states_scale is not None else None,
+                ptr_array([x.data_ptr() for x in topk_ids]),
+                ptr_array([x.data_ptr() for x in topk_weights]) if topk_weights is not None else None,
+                c_counts, rt, _mask_value(active_rank_mask), ctypes.c_void_p(_stream_ptr(self.device)),
+                ctypes.byref(res)))
+        T = res.tokens_per_rank
+        rows = ep * T
+        self._counts, self._T = counts, T
+        hs = [self._view(res.recv_hidden[d], rows, H, self.dtype) for d in range(ep)]
+        ids = [self._view(res.recv_topk_ids[d], rows, K, torch.int32) for d in range(ep)]
+        sc = [self._view(res.recv_scale[d], rows, G, torch.float32) for d in range(ep)] \
+            if res.recv_scale else None
+        w = [self._view(res.recv_topk_weights[d], rows, K, torch.float32) for d in range(ep)] \
+            if res.recv_topk_weights else None
+        return EpDispatchResult(T, hs, sc, ids, w)
+
+    # -- MoEEpCommunication.get_combine_input_buffer ------------------------
+    def get_combine_input_buffer(self, dtype: torch.dtype = torch.bfloat16, *, rank: Optional[int] = None):
+        """Rank ``rank``'s bf16 [ep_size*tokens_per_rank, hidden] combine input
+        (all ranks as a list when ``rank`` is None); None for other dtypes.
+        Valid only between dispatch() and combine()."""
+        self._live()
+        if dtype != torch.bfloat16:
+            return None
+        ranks = range(self.ep_size) if rank is None else [int(rank)]
+        out = []
+        for r in ranks:
+            p = ctypes.c_void_p()
+            check(self._L.ep_get_combine_input_buffer(self._h, r, ctypes.byref(p)))
+            out.append(self._view(p.value, self.ep_size * self._T, self.hidden, torch.bfloat16))
+        return out if rank is None else out[0]
+
+    # -- MoEEpCommunication.combine -----------------------------------------
+    def combine(self, expert_output: Optional[Sequence[Optional[torch.Tensor]]] = None, *,
+                output: Optional[Sequence[torch.Tensor]] = None,
+                active_rank_mask=None) -> List[torch.Tensor]:
+        """Per source rank, bf16 [n_s, hidden]: the sum over the ranks each
+        token was routed to (ascending, fp32) of their expert_output rows.
+
+        ``expert_output[d]`` is rank d's bf16 [ep_size*tokens_per_rank, hidden]
+        (or [ep_size, tokens_per_rank, hidden]) tensor; None, or a None entry,
+        means the backend combine input buffer (no copy)."""
+        self._live()
+        ep, H = self.ep_size, self.hidden
+        if self._counts is None:
+            raise EpError(_lib.EP_ERR_STATE, "combine called without a pending dispatch")
+        rows = ep * self._T
+        eo_ptrs = None
+        if expert_output is not None:
+            if len(expert_output) != ep:
+                raise ValueError(f"expert_output needs {ep} per-rank tensors")
+            eo_ptrs = []
+            for d, e in enumerate(expert_output):
+                if e is None:
+                    eo_ptrs.append(0)
+                    continue
+                if e.dtype != torch.bfloat16 or e.device != self.device or not e.is_contiguous() \
+                        or e.numel() != rows * H or e.shape[-1] != H:
+                    raise ValueError(f"expert_output[{d}] must be contiguous bf16 [{rows}, {H}] on "
+                                     f"{self.device}")
+                eo_ptrs.append(e.data_ptr())
+        if output is None:
+            output = [torch.empty(n, H, dtype=torch.bfloat16, device=self.device) for n in self._counts]
+        else:
+            if len(output) != ep:
+                raise ValueError(f"output needs {ep} per-rank tensors")
+            for s in range(ep):
+                self._check_rank_tensor("output", output[s], s, self._counts[s], H, torch.bfloat16)
+        with torch.cuda.device(self.device):
+            check(self._L.ep_combine(self._h, ptr_array(eo_ptrs) if eo_ptrs is not None else None,
+                                     ptr_array([o.data_ptr() for o in output]),
+                                     _mask_value(active_rank_mask),
+                                     ctypes.c_void_p(_stream_ptr(self.device))))
+        self._counts = None
+        return list(output)
+
+    # -- MoEEpCommunication.destroy -----------------------------------------
+    def destroy(self) -> None:
+        """Release the handle and workspace; calling it again does nothing."""
+        if self._h is None:
+            return
+        torch.cuda.synchronize(self.device)
+        check(self._L.ep_destroy(self._h))
+        self._h = None
+        self._ws = None
+
+    def __del__(self):
+        try:
+            if getattr(self, "_h", None) is not None:
+                self._L.ep_destroy(self._h)
+                self._h = None
+        except Exception:
+            pass

@@ -1,0 +1,177 @@
+/*
+ * ep.h -- C ABI of the GB300 (sm_103a) rank-major MoE expert-parallel
+ * dispatch/combine library (libep_gb300.so).
+ *
+ * The operation is the one FlashInfer's moe_ep API pages define:
+ *  - page "flashinfer.moe_ep.MoEEpCommunication": dispatch() sends each token
+ *    to the ranks that own its selected experts; combine() returns each
+ *    token's expert outputs summed over ranks; get_combine_input_buffer()
+ *    hands out a backend-owned buffer the expert computation may write into;
+ *    one dispatch() is followed by exactly one combine(); destroy() is
+ *    idempotent.
+ *  - page "flashinfer.moe_ep.NVLinkOneSidedAlltoAll": hidden rows, scales,
+ *    topk_ids and topk_weights travel as payloads of one dispatch; receive
+ *    row source_rank*tokens_per_rank+token holds that token; padding rows and
+ *    rows of tokens not routed to a rank get invalid_expert_id routing;
+ *    active_rank_mask drops tokens routed to masked-off ranks and must be the
+ *    same on dispatch and combine.
+ *
+ * All ep_size ranks of the EP group are virtual ranks on ONE GPU: every
+ * rank's inputs, receive buffers and combine inputs live in that GPU's
+ * memory, and one call handles all ranks at once. The per-rank arguments
+ * are therefore host arrays of ep_size device pointers, entry r belonging
+ * to rank r.
+ *
+ * Readings the pages leave open, fixed here:
+ *  - invalid_expert_id is EP_INVALID_EXPERT_ID (-1); ids are int32, weights
+ *    and scales fp32; a scale row has hidden/128 entries.
+ *  - experts are split contiguously: rank d owns ids [d*E/ep, (d+1)*E/ep);
+ *    ids outside [0, E) route nowhere; duplicate ids reach a rank once.
+ *  - a routed receive row carries the token's whole top-k id row unchanged;
+ *    only the id row of a padding/unrouted row is defined (all -1); its
+ *    hidden, scale and weight rows keep whatever they held.
+ *  - the rank mask filters destinations only.
+ *  - combine adds, per token, the rows of the ranks it was routed to, in
+ *    ascending rank order, in fp32 from +0.0, and rounds once to bf16
+ *    (round to nearest even). The result is bit-exact and deterministic.
+ *
+ * Errors are synchronous: each call checks its arguments and the handle's
+ * state on the host before it launches anything, and returns a status;
+ * ep_last_error() gives a message. GPU work is queued on the given stream
+ * (NULL = the legacy default stream) and is asynchronous to the host.
+ */
+#ifndef EP_GB300_H
+#define EP_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    EP_OK = 0,
+    EP_ERR_INVALID_ARG = 1, /* bad sizes, pointers, masks, or weights/scales on some ranks only */
+    EP_ERR_STATE = 2,       /* dispatch while one is pending, combine without dispatch */
+    EP_ERR_CUDA = 3,        /* a CUDA runtime call failed (message has the CUDA error) */
+    EP_ERR_OOM = 4,         /* workspace allocation failed */
+    EP_ERR_UNSUPPORTED = 5  /* no sm_103 device current */
+} ep_status;
+
+typedef enum {
+    EP_DTYPE_BF16 = 0,     /* hidden rows of bfloat16 */
+    EP_DTYPE_FP8_E4M3 = 1  /* hidden rows of OCP fp8 e4m3fn */
+} ep_dtype;
+
+#define EP_INVALID_EXPERT_ID (-1)
+#define EP_MAX_EP_SIZE 64 /* the rank mask is one uint64 */
+#define EP_MAX_TOP_K 32
+#define EP_SCALE_GROUP 128 /* hidden columns per fp32 scale */
+
+typedef struct ep_handle ep_handle;
+
+/* Where one dispatch left its results. All arrays are host arrays owned by
+ * the handle, each with ep_size device pointers (entry d = destination rank
+ * d). Buffer d holds ep_size*tokens_per_rank rows; row s*tokens_per_rank+t
+ * is token t of source rank s. The pointers stay valid until ep_destroy; the
+ * contents until the next ep_dispatch. */
+typedef struct {
+    int tokens_per_rank;
+    int ep_size;
+    void *const *recv_hidden;         /* rows of `hidden` elements of the payload dtype */
+    float *const *recv_scale;         /* rows of hidden/128 fp32, or NULL if none were sent */
+    int32_t *const *recv_topk_ids;    /* rows of top_k int32 */
+    float *const *recv_topk_weights;  /* rows of top_k fp32, or NULL if none were sent */
+} ep_dispatch_result;
+
+/* 1 when the current CUDA device can run this library (compute capability
+ * 10.3, the sm_103a build), else 0. Does no GPU work.
+ * (MoEEpCommunication.is_platform_supported) */
+int ep_is_supported(void);
+
+/* Bytes of device workspace a handle with these parameters needs: for every
+ * rank, receive buffers and a bf16 combine-input buffer of ep_size *
+ * max_tokens_per_rank rows, plus 8 bytes of routing state per slot.
+ * Validates the parameters like ep_create. */
+ep_status ep_workspace_size(int ep_size, int num_experts, int top_k, int hidden,
+                            int max_tokens_per_rank, ep_dtype dtype, size_t *bytes);
+
+/* Creates a handle for one EP group (MoEEpCommunication constructor with
+ * MoEEpCommParams). Requirements: 1 <= ep_size <= 64; num_experts a
+ * positive multiple of ep_size; 1 <= top_k <= 32; hidden > 0 with
+ * hidden*elem_bytes a multiple of 16; max_tokens_per_rank >= 0.
+ * enable_rank_mask (0/1) allows active_rank_mask on dispatch/combine.
+ * Allocates the workspace with cudaMalloc on the current device; *out
+ * receives the handle (NULL on error). */
+ep_status ep_create(int ep_size, int num_experts, int top_k, int hidden,
+                    int max_tokens_per_rank, ep_dtype dtype, int enable_rank_mask,
+                    ep_handle **out);
+
+/* As ep_create, but uses caller-owned device memory `workspace` of `bytes`
+ * (>= ep_workspace_size, 256-byte aligned) on the current device. The
+ * caller frees it after ep_destroy. */
+ep_status ep_create_with_workspace(int ep_size, int num_experts, int top_k, int hidden,
+                                   int max_tokens_per_rank, ep_dtype dtype, int enable_rank_mask,
+                                   void *workspace, size_t bytes, ep_handle **out);
+
+/* Dispatch of all ep_size source ranks (MoEEpCommunication.dispatch;
+ * NVLinkOneSidedAlltoAll.dispatch for active_rank_mask).
+ *  hidden[s]       device [num_tokens[s], hidden] payload dtype, 16-byte aligned
+ *  hidden_scale    NULL, or hidden_scale[s] device fp32 [num_tokens[s], hidden/128]
+ *                  (needs hidden % 128 == 0)
+ *  topk_ids[s]     device int32 [num_tokens[s], top_k], global expert ids
+ *  topk_weights    NULL, or topk_weights[s] device fp32 [num_tokens[s], top_k]
+ *  num_tokens      host int32 [ep_size], 0 <= num_tokens[s] <= tokens_per_rank
+ *  runtime_max_tokens_per_rank  tokens_per_rank of this step, <= max_tokens_per_rank;
+ *                  negative means max_tokens_per_rank (static shapes)
+ *  active_rank_mask  bit d set = rank d active; UINT64_MAX = all ranks. Any
+ *                  other value needs a handle created with enable_rank_mask and
+ *                  no bit at or above ep_size (else EP_ERR_INVALID_ARG).
+ *  stream          cudaStream_t to queue the work on
+ *  out             filled with the receive buffers (may be NULL)
+ * Scales and weights are all-or-none: if the array is given, every rank with
+ * tokens must pass a non-NULL pointer (an empty rank may pass anything).
+ * Rows of ranks with zero tokens are never read. Inputs must stay valid until
+ * the queued work has run. Returns EP_ERR_STATE if a dispatch is pending. */
+ep_status ep_dispatch(ep_handle *h, const void *const *hidden, const float *const *hidden_scale,
+                      const int32_t *const *topk_ids, const float *const *topk_weights,
+                      const int32_t *num_tokens, int runtime_max_tokens_per_rank,
+                      uint64_t active_rank_mask, void *stream, ep_dispatch_result *out);
+
+/* Device pointer to rank `rank`'s backend-owned combine input: bf16
+ * [ep_size*tokens_per_rank, hidden] of the pending dispatch. Passing it (or
+ * NULL) to ep_combine saves a copy. Valid between ep_dispatch and
+ * ep_combine; EP_ERR_STATE outside (MoEEpCommunication.get_combine_input_buffer,
+ * NVLinkOneSidedAlltoAll.get_combine_input_buffer). */
+ep_status ep_get_combine_input_buffer(ep_handle *h, int rank, void **out);
+
+/* Combine of the pending dispatch (MoEEpCommunication.combine).
+ *  expert_output   NULL = every rank's backend combine input buffer; else
+ *                  expert_output[d] is rank d's bf16 [ep_size*tokens_per_rank,
+ *                  hidden] device buffer (NULL entry = that rank's backend
+ *                  buffer), 16-byte aligned; only routed rows are read.
+ *  output[s]       device bf16 [num_tokens[s], hidden], 16-byte aligned,
+ *                  caller-owned; may be NULL when num_tokens[s] == 0.
+ *  active_rank_mask  must equal the dispatch's (when masking is enabled).
+ * output[s][t] = bf16( sum over routed ranks d ascending of expert_output[d]
+ * [s*tokens_per_rank + t] ) with an fp32 accumulator from +0.0. A token
+ * routed nowhere gets +0.0. Returns the handle to the idle state. */
+ep_status ep_combine(ep_handle *h, const void *const *expert_output, void *const *output,
+                     uint64_t active_rank_mask, void *stream);
+
+/* Frees the handle and (if ep_create allocated it) its workspace after
+ * synchronising the device. NULL is a no-op (MoEEpCommunication.destroy). */
+ep_status ep_destroy(ep_handle *h);
+
+/* Bit set of the listed ranks, for active_rank_mask; ranks outside [0, 64)
+ * are ignored (NVLinkOneSidedAlltoAll.active_rank_mask). */
+uint64_t ep_rank_mask(const int *ranks, int n);
+
+/* Message of the calling thread's last failed call ("" if none). */
+const char *ep_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* EP_GB300_H */

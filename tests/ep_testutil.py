@@ -39,3 +39,105 @@ def small(wl, hidden=256, tokens=None):
         counts = ("fixed",) + tuple(min(c, rt or cap) for c in counts[1:])
     return wl.replace(name=wl.name + "_small", hidden=hidden, capacity=cap, runtime_max=rt,
                       counts=counts)
+
+
+# ---------------------------------------------------------------------------
+# GPU round trip through the library, and the matching oracle computation
+# ---------------------------------------------------------------------------
+EO_SEED = 7
+
+
+def to_dev(lst, device):
+    return None if lst is None else [x.to(device) for x in lst]
+
+
+def fill_expert_outputs(comm, T, device, seed=EO_SEED, special=False, caller=False):
+    """Writes the stand-in expert outputs of every rank: into the backend
+    combine-input buffers, or (caller=True) into fresh tensors it returns."""
+    import workloads
+    ep, H = comm.ep_size, comm.hidden
+    rows = torch.arange(ep * T, device=device)
+    outs = []
+    for d in range(ep):
+        eo = workloads.expert_output_rows(seed, d, rows, H, device=device, special=special)
+        if caller:
+            outs.append(eo.contiguous())
+        else:
+            comm.get_combine_input_buffer(rank=d).copy_(eo)
+    return outs if caller else None
+
+
+def gpu_round(inp, device, special=False, caller_eo=False, comm=None, keep=False):
+    """dispatch + (stand-in expert) + combine of ``inp`` through EpComm.
+    Returns host copies of the receive buffers and outputs."""
+    from combine_topk_ids_dest_gb300 import EpComm
+    wl = inp.wl
+    dtype = torch.bfloat16 if wl.dtype == "bf16" else torch.float8_e4m3fn
+    own = comm is None
+    if own:
+        comm = EpComm(wl.ep_size, wl.num_experts, wl.top_k, wl.hidden, wl.capacity, dtype=dtype,
+                      enable_rank_mask=wl.enable_rank_mask, device=device)
+    mask = inp.active_rank_mask if wl.enable_rank_mask else None
+    res = comm.dispatch(to_dev(inp.hidden, device), to_dev(inp.topk_ids, device),
+                        to_dev(inp.topk_weights, device),
+                        hidden_states_scale=to_dev(inp.scale, device),
+                        runtime_max_tokens_per_rank=wl.runtime_max, active_rank_mask=mask)
+    T = res.tokens_per_rank
+    eo = fill_expert_outputs(comm, T, device, special=special, caller=caller_eo)
+    out = comm.combine(eo, active_rank_mask=mask)
+    torch.cuda.synchronize(device)
+    host = dict(
+        T=T,
+        recv_ids=[x.cpu().numpy() for x in res.topk_ids],
+        recv_hidden=[raw_bytes(x.cpu()) for x in res.hidden_states],
+        recv_scale=None if res.hidden_states_scale is None else
+        [x.cpu().numpy() for x in res.hidden_states_scale],
+        recv_weights=None if res.topk_weights is None else [x.cpu().numpy() for x in res.topk_weights],
+        out=[bf16_bits(o.cpu()) for o in out],
+    )
+    if own and not keep:
+        comm.destroy()
+    if keep:
+        host["comm"] = comm
+    return host
+
+
+def oracle_round(inp, special=False):
+    """The oracle's dispatch and combine of ``inp`` with the same stand-in
+    expert outputs (generated on the CPU)."""
+    import oracle
+    import workloads
+    wl = inp.wl
+    T, ep, H = wl.tokens_per_rank, wl.ep_size, wl.hidden
+    disp = oracle.dispatch(ep, wl.num_experts, wl.top_k, T, inp.num_tokens, inp.hidden, inp.topk_ids,
+                           scale=inp.scale, topk_weights=inp.topk_weights,
+                           mask_enabled=wl.enable_rank_mask, active_rank_mask=inp.active_rank_mask)
+    rows = torch.arange(ep * T)
+    eo = [bf16_bits(workloads.expert_output_rows(EO_SEED, d, rows, H, special=special))
+          for d in range(ep)]
+    out = oracle.combine(ep, wl.num_experts, wl.top_k, H, T, inp.num_tokens, inp.topk_ids, eo,
+                         mask_enabled=wl.enable_rank_mask, active_rank_mask=inp.active_rank_mask)
+    return disp, out
+
+
+def assert_round_equal(inp, got, disp, out):
+    """Bit-exact comparison: every id row; hidden/scale/weight rows where the
+    oracle's id row is valid (the others are unspecified); every output."""
+    wl = inp.wl
+    for d in range(wl.ep_size):
+        np.testing.assert_array_equal(got["recv_ids"][d], disp.recv_ids[d], err_msg=f"ids of rank {d}")
+        valid = (disp.recv_ids[d] != INV).any(axis=1)  # a routed row holds an id owned by d
+        np.testing.assert_array_equal(got["recv_hidden"][d][valid], disp.recv_hidden[d][valid],
+                                      err_msg=f"hidden rows of rank {d}")
+        if disp.recv_scale is not None:
+            np.testing.assert_array_equal(got["recv_scale"][d][valid].view(np.uint32),
+                                          disp.recv_scale[d][valid].view(np.uint32))
+        else:
+            assert got["recv_scale"] is None
+        if disp.recv_weights is not None:
+            np.testing.assert_array_equal(got["recv_weights"][d][valid].view(np.uint32),
+                                          disp.recv_weights[d][valid].view(np.uint32))
+        else:
+            assert got["recv_weights"] is None
+    for s in range(wl.ep_size):
+        np.testing.assert_array_equal(got["out"][s], out[s], err_msg=f"combine output of rank {s}")

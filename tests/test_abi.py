@@ -1,0 +1,105 @@
+"""CPU checks of the C ABI: the library builds for sm_103a, loads, exports
+every function include/ep.h declares, and its host-only entry points behave
+(argument validation, workspace sizing, rank masks) without a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import combine_topk_ids_dest_gb300 as ep
+from combine_topk_ids_dest_gb300 import _lib
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "ep.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ep_[a-z_]+)\s*\(", text)))
+
+
+def test_header_and_exports_agree():
+    decl = declared_functions()
+    assert decl == sorted(_lib.EXPORTS)
+    L = _lib.load()
+    for name in decl:
+        assert hasattr(L, name), name
+
+
+def test_library_is_built_for_sm103a():
+    path = _lib.load()._name
+    assert os.path.basename(path) == "libep_gb300.so"
+    assert os.path.dirname(path).endswith(os.path.join("combine_topk_ids_dest_gb300", "_build"))
+
+
+def _size(*args):
+    n = ctypes.c_size_t(0)
+    st = _lib.load().ep_workspace_size(*args, ctypes.byref(n))
+    return st, n.value
+
+
+def _align(x):
+    return (x + 255) // 256 * 256
+
+
+@pytest.mark.parametrize("ep_size,E,K,H,C,dt", [(32, 256, 8, 7168, 1024, 1), (8, 8, 2, 4096, 256, 0),
+                                                (2, 8, 2, 256, 16, 0), (3, 6, 3, 136, 5, 0),
+                                                (4, 8, 2, 256, 0, 0)])
+def test_workspace_size_formula(ep_size, E, K, H, C, dt):
+    st, n = _size(ep_size, E, K, H, C, dt)
+    assert st == ep.EP_OK
+    rows = ep_size * C
+    elem = 2 if dt == 0 else 1
+    G = H // 128 if H % 128 == 0 else 0
+    want = ep_size * (_align(rows * H * elem) + _align(rows * G * 4) + _align(rows * K * 4) * 2 +
+                      _align(rows * H * 2)) + _align(rows * 8)
+    assert n == max(want, 256)
+
+
+@pytest.mark.parametrize("args,frag", [
+    ((0, 8, 2, 256, 16, 0), "ep_size"),
+    ((65, 65, 2, 256, 16, 0), "ep_size"),
+    ((3, 8, 2, 256, 16, 0), "multiple"),
+    ((2, 8, 0, 256, 16, 0), "top_k"),
+    ((2, 8, 33, 256, 16, 0), "top_k"),
+    ((2, 8, 2, 12, 16, 0), "16 bytes"),
+    ((2, 8, 2, 8, 16, 1), "16 bytes"),
+    ((2, 8, 2, 256, -1, 0), "max_tokens_per_rank"),
+    ((2, 8, 2, 256, 16, 7), "dtype"),
+])
+def test_workspace_size_rejects(args, frag):
+    st, _ = _size(*args)
+    assert st == ep.EP_ERR_INVALID_ARG
+    assert frag in _lib.load().ep_last_error().decode()
+
+
+def test_rank_mask_helper():
+    L = _lib.load()
+    arr = (ctypes.c_int * 5)(0, 3, 63, 64, -1)
+    assert L.ep_rank_mask(arr, 5) == (1 | (1 << 3) | (1 << 63))
+    assert int(ep.EpComm.active_rank_mask([1, 2]).item()) == 6
+
+
+def test_null_handle_calls_fail_cleanly():
+    L = _lib.load()
+    assert L.ep_destroy(None) == ep.EP_OK
+    res = _lib.EpDispatchResultC()
+    assert L.ep_dispatch(None, None, None, None, None, None, -1, 0, None, ctypes.byref(res)) == \
+        ep.EP_ERR_INVALID_ARG
+    assert L.ep_combine(None, None, None, 0, None) == ep.EP_ERR_INVALID_ARG
+    p = ctypes.c_void_p()
+    assert L.ep_get_combine_input_buffer(None, 0, ctypes.byref(p)) == ep.EP_ERR_INVALID_ARG
+
+
+def test_create_without_gpu_reports_error():
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    L = _lib.load()
+    h = ctypes.c_void_p(1)
+    st = L.ep_create(2, 8, 2, 256, 16, 0, 0, ctypes.byref(h))
+    assert st in (ep.EP_ERR_CUDA, ep.EP_ERR_UNSUPPORTED)
+    assert h.value is None
+    assert L.ep_is_supported() == 0
+    assert not ep.EpComm.is_platform_supported()

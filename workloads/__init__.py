@@ -197,10 +197,12 @@ def make_inputs(wl: EpWorkload) -> EpInputs:
             hidden.append(x.to(torch.bfloat16).contiguous())
             if wl.scales:
                 scale.append(torch.rand(n, wl.scale_cols, generator=g).to(torch.float32) + 0.5)
-        else:
+        elif wl.scales:
             q, s = quantize_fp8_groups(x)
             hidden.append(q)
             scale.append(s)
+        else:  # fp8 rows without scales: N(0,1) values cast directly
+            hidden.append(x.clamp(-FP8_MAX, FP8_MAX).to(torch.float8_e4m3fn).contiguous())
     if wl.enable_rank_mask:
         mask = rank_bits(wl.active_ranks())
     else:
