@@ -113,6 +113,14 @@ def recorded_traffic(kernel: str, workload: str):
     return None
 
 
+class _Null:
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        return False
+
+
 class ClockSampler:
     """nvidia-smi clock/throttle samples every 200 ms while the timed region runs."""
 
@@ -174,6 +182,22 @@ class ClockSampler:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
                 "samples": len(sm), "power_w_max": max(power) if power else None}
+
+
+def reduce_max(values, device=None):
+    """Element-wise max over all ranks of the default process group (identity
+    without one): the slowest replica sets the time of the whole job."""
+    import torch.distributed as dist
+    if not dist.is_available() or not dist.is_initialized() or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def whole_job_gbs(bytes_per_round: int, rounds: int, world: int, max_total_ms: float) -> float:
+    """GB/s of the whole job: every replica's bytes over the slowest replica's time."""
+    return world * bytes_per_round * rounds / (max_total_ms / 1e3) / 1e9
 
 
 # ---------------------------------------------------------------------------
@@ -314,31 +338,44 @@ def run_ours(args, rank, world):
     combine()
     launches_per_round = 2 if wl.ep_size * wl.tokens_per_rank > 0 else 0
 
-    for i in range(args.warmup):
-        flush.fill_(i & 0xFF)
+    # The same two API calls captured once in CUDA graphs (static shapes):
+    # replaying them runs exactly the dispatch and combine kernels, without
+    # the Python binding's per-call overhead in the measured device time.
+    g_disp, g_comb = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_disp):
         dispatch()
+    with torch.cuda.graph(g_comb):
         combine()
-    torch.cuda.synchronize(dev)
-    if world > 1:
-        dist.barrier()
 
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
-    with ClockSampler(dev) as clocks:
+    def timed_rounds(run_dispatch, run_combine, steps, warmup, clocks=None):
+        for i in range(warmup):
+            flush.fill_(i & 0xFF)
+            run_dispatch()
+            run_combine()
         torch.cuda.synchronize(dev)
-        for i in range(args.steps):
-            flush.fill_((i + 1) & 0xFF)
-            ev[i][0].record()
-            dispatch()
-            ev[i][1].record()
-            combine()
-            ev[i][2].record()
-        torch.cuda.synchronize(dev)
-    if world > 1:
-        dist.barrier()
-    t_disp = [e[0].elapsed_time(e[1]) for e in ev]
-    t_comb = [e[1].elapsed_time(e[2]) for e in ev]
-    t_round = [e[0].elapsed_time(e[2]) for e in ev]
+        if world > 1:
+            dist.barrier()
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+        with (clocks if clocks is not None else _Null()):
+            torch.cuda.synchronize(dev)
+            for i in range(steps):
+                flush.fill_((i + 1) & 0xFF)
+                ev[i][0].record()
+                run_dispatch()
+                ev[i][1].record()
+                run_combine()
+                ev[i][2].record()
+            torch.cuda.synchronize(dev)
+        if world > 1:
+            dist.barrier()
+        return ([e[0].elapsed_time(e[1]) for e in ev], [e[1].elapsed_time(e[2]) for e in ev],
+                [e[0].elapsed_time(e[2]) for e in ev])
+
+    clocks = ClockSampler(dev)
+    t_disp, t_comb, t_round = timed_rounds(g_disp.replay, g_comb.replay, args.steps, args.warmup, clocks)
     total_ms = sum(t_round)
+    ed, ec, er = timed_rounds(dispatch, combine, args.steps, args.warmup)
+    eager_ms = sum(er)
 
     # end to end through the public API from pinned host memory
     pin = lambda lst: None if lst is None else [x.pin_memory() for x in lst]
@@ -367,17 +404,14 @@ def run_ours(args, rank, world):
     torch.cuda.synchronize(dev)
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
 
-    if world > 1:
-        t = torch.tensor([total_ms, e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms, e2e_ms = float(t[0]), float(t[1])
+    total_ms, e2e_ms, eager_ms = reduce_max([total_ms, e2e_ms, eager_ms], device=dev)
     comm.destroy()
     if rank != 0:
         return
 
     peak, peak_src = hbm_peak()
     ms = total_ms / args.steps
-    gbs = world * b["total"] * args.steps / (total_ms / 1e3) / 1e9
+    gbs = whole_job_gbs(b["total"], args.steps, world, total_ms)
     disp_ms, comb_ms = statistics.mean(t_disp), statistics.mean(t_comb)
     kernels = {
         "dispatch_kernel": {"bytes": b["dispatch"], "ms": disp_ms},
@@ -398,9 +432,15 @@ def run_ours(args, rank, world):
         "roofline": {"bound": "hbm", "kernel": top, "achieved": per[top]["achieved"], "peak": peak,
                      "unit": "GB/s", "frac": per[top]["frac"], "traffic": per[top]["traffic"],
                      "peak_source": peak_src, "kernels": per},
-        "e2e": {"value": world * b["total"] / (e2e_ms / 1e3) / 1e9, "unit": "GB/s", "ms_per_step": e2e_ms,
+        "e2e": {"value": whole_job_gbs(b["total"], 1, world, e2e_ms), "unit": "GB/s", "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": b["h2d"], "d2h_bytes_per_step": b["d2h"], "steps": e2e_steps,
                 "path": "pinned host inputs -> H2D -> EpComm.dispatch/combine (C ABI) -> D2H outputs"},
+        "eager": {"value": whole_job_gbs(b["total"], args.steps, world, eager_ms), "unit": "GB/s",
+                  "ms_per_step": eager_ms / args.steps,
+                  "dispatch_ms": statistics.mean(ed), "combine_ms": statistics.mean(ec),
+                  "path": "EpComm.dispatch/combine called from Python each round"},
+        "timing": "CUDA-graph replay of the captured EpComm.dispatch and EpComm.combine calls; "
+                  "events on the launching stream around each",
         "gpu_launches": launches_per_round * args.steps,
         "clocks": clocks.summary(),
     }
@@ -428,10 +468,23 @@ def main():
     ap.add_argument("--reference-seconds", type=float, default=120.0,
                     help="total oracle time of the reference arm")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tokens-per-rank", type=int, default=None,
+                    help="shrink the workload to this many tokens per rank (profiling runs only)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
 
+    if args.tokens_per_rank is not None:
+        wl = workloads.WORKLOADS[args.workload]
+        m = args.tokens_per_rank
+        counts = wl.counts
+        if counts[0] == "uniform":
+            counts = ("uniform", min(counts[1], m), min(counts[2], m))
+        elif counts[0] == "fixed":
+            counts = ("fixed",) + tuple(min(c, m) for c in counts[1:])
+        workloads.WORKLOADS[args.workload] = wl.replace(
+            name=f"{wl.name}_T{m}", capacity=m, runtime_max=None if wl.runtime_max is None else m,
+            counts=counts)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if args.impl == "reference":

@@ -90,6 +90,8 @@ class EpComm:
         self._h = h
         self._counts: Optional[List[int]] = None
         self._T = 0
+        self._dev_index = self.device.index if self.device.index is not None else torch.cuda.current_device()
+        self._views = {}  # (kind, T) -> per-rank views of the workspace
 
     # -- MoEEpCommunication.is_platform_supported ---------------------------
     @classmethod
@@ -116,13 +118,20 @@ class EpComm:
             raise EpError(_lib.EP_ERR_STATE, "the communicator was destroyed")
 
     def _check_rank_tensor(self, name, t, s, n, cols, dtype):
-        if t.device != self.device:
-            raise ValueError(f"{name}[{s}] is on {t.device}, expected {self.device}")
-        if t.dtype != dtype:
-            raise ValueError(f"{name}[{s}] has dtype {t.dtype}, expected {dtype}")
-        if t.dim() != 2 or t.shape[0] != n or t.shape[1] != cols or not t.is_contiguous():
+        if t.dtype is not dtype or not t.is_cuda or t.get_device() != self._dev_index:
+            raise ValueError(f"{name}[{s}] is {t.dtype} on {t.device}, expected {dtype} on {self.device}")
+        if t.shape != (n, cols) or not t.is_contiguous():
             raise ValueError(f"{name}[{s}] must be a contiguous [{n}, {cols}] tensor, got "
                              f"{tuple(t.shape)}")
+
+    def _rank_views(self, kind, ptrs, T, cols, dtype):
+        key = (kind, T)
+        v = self._views.get(key)
+        if v is None:
+            rows = self.ep_size * T
+            v = [self._view(ptrs[d], rows, cols, dtype) for d in range(self.ep_size)]
+            self._views[key] = v
+        return list(v)
 
     # -- MoEEpCommunication.dispatch ----------------------------------------
     def dispatch(self, hidden_states: Sequence[torch.Tensor], topk_ids: Sequence[torch.Tensor],
@@ -173,13 +182,11 @@ class EpComm:
                 c_counts, rt, _mask_value(active_rank_mask), ctypes.c_void_p(_stream_ptr(self.device)),
                 ctypes.byref(res)))
         T = res.tokens_per_rank
-        rows = ep * T
         self._counts, self._T = counts, T
-        hs = [self._view(res.recv_hidden[d], rows, H, self.dtype) for d in range(ep)]
-        ids = [self._view(res.recv_topk_ids[d], rows, K, torch.int32) for d in range(ep)]
-        sc = [self._view(res.recv_scale[d], rows, G, torch.float32) for d in range(ep)] \
-            if res.recv_scale else None
-        w = [self._view(res.recv_topk_weights[d], rows, K, torch.float32) for d in range(ep)] \
+        hs = self._rank_views("hidden", res.recv_hidden, T, H, self.dtype)
+        ids = self._rank_views("ids", res.recv_topk_ids, T, K, torch.int32)
+        sc = self._rank_views("scale", res.recv_scale, T, G, torch.float32) if res.recv_scale else None
+        w = self._rank_views("weights", res.recv_topk_weights, T, K, torch.float32) \
             if res.recv_topk_weights else None
         return EpDispatchResult(T, hs, sc, ids, w)
 
@@ -196,7 +203,12 @@ class EpComm:
         for r in ranks:
             p = ctypes.c_void_p()
             check(self._L.ep_get_combine_input_buffer(self._h, r, ctypes.byref(p)))
-            out.append(self._view(p.value, self.ep_size * self._T, self.hidden, torch.bfloat16))
+            key = ("combine_in", r, self._T)
+            v = self._views.get(key)
+            if v is None:
+                v = self._views[key] = self._view(p.value, self.ep_size * self._T, self.hidden,
+                                                  torch.bfloat16)
+            out.append(v)
         return out if rank is None else out[0]
 
     # -- MoEEpCommunication.combine -----------------------------------------
@@ -223,8 +235,8 @@ class EpComm:
                 if e is None:
                     eo_ptrs.append(0)
                     continue
-                if e.dtype != torch.bfloat16 or e.device != self.device or not e.is_contiguous() \
-                        or e.numel() != rows * H or e.shape[-1] != H:
+                if e.dtype is not torch.bfloat16 or not e.is_cuda or e.get_device() != self._dev_index \
+                        or not e.is_contiguous() or e.numel() != rows * H or e.shape[-1] != H:
                     raise ValueError(f"expert_output[{d}] must be contiguous bf16 [{rows}, {H}] on "
                                      f"{self.device}")
                 eo_ptrs.append(e.data_ptr())
@@ -251,6 +263,7 @@ class EpComm:
         torch.cuda.synchronize(self.device)
         check(self._L.ep_destroy(self._h))
         self._h = None
+        self._views = {}
         self._ws = None
 
     def __del__(self):

@@ -152,23 +152,29 @@ def dispatch(ep_size: int, num_experts: int, top_k: int, tokens_per_rank: int,
              num_tokens: Sequence[int], hidden: Sequence, topk_ids: Sequence, *,
              scale: Optional[Sequence] = None, topk_weights: Optional[Sequence] = None,
              mask_enabled: bool = False, active_rank_mask: int = (1 << 64) - 1,
-             payload: bool = True) -> OracleDispatch:
+             payload: bool = True, row_bytes: Optional[int] = None,
+             scale_cols: Optional[int] = None) -> OracleDispatch:
     """Receive buffers of every rank after one dispatch (see ep_oracle.c).
 
     ``hidden[s]`` is [n_s, H] bf16/fp8 (raw bytes are copied); ``scale[s]``
     [n_s, G] fp32; ``topk_ids[s]`` [n_s, K] int32; ``topk_weights[s]`` [n_s, K]
     fp32. Rows the method leaves unspecified keep the sentinel fill. With
-    ``payload=False`` only the id planes are produced.
+    ``payload=False`` only the id planes are produced. ``row_bytes`` (hidden
+    row bytes) and ``scale_cols`` are taken from the data when omitted; pass
+    them when every rank is empty.
     """
     ep, T, K = ep_size, tokens_per_rank, top_k
     counts = np.ascontiguousarray(np.asarray(num_tokens, dtype=np.int32))
     hid = [_np(h) for h in hidden]
     hid = [h.view(np.uint8).reshape(h.shape[0], -1) if h.size else h.reshape(0, 0).view(np.uint8)
            for h in hid]
-    row_bytes = max((h.shape[1] for h in hid if h.size), default=0)
+    if row_bytes is None:  # from the data; pass it when every rank is empty
+        row_bytes = max((h.shape[1] for h in hid if h.size), default=0)
     ids = [_np(i, np.int32) for i in topk_ids]
     sc = [_np(x, np.float32) for x in scale] if scale is not None else None
-    G = max((x.shape[1] for x in sc if x.size), default=0) if sc is not None else 0
+    G = 0
+    if sc is not None:
+        G = scale_cols if scale_cols is not None else max((x.shape[1] for x in sc if x.size), default=0)
     w = [_np(x, np.float32) for x in topk_weights] if topk_weights is not None else None
 
     rows = ep * T

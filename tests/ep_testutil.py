@@ -20,6 +20,8 @@ def raw_bytes(t):
     """uint8 numpy [n, row_bytes] of a bf16 / fp8 / any CPU tensor."""
     t = t.detach().contiguous()
     n = t.shape[0]
+    if n == 0:
+        return np.zeros((0, t[0:0].view(-1).element_size() * (t.shape[1] if t.dim() > 1 else 1)), np.uint8)
     return t.view(torch.uint8).numpy().reshape(n, -1)
 
 
@@ -111,7 +113,8 @@ def oracle_round(inp, special=False):
     T, ep, H = wl.tokens_per_rank, wl.ep_size, wl.hidden
     disp = oracle.dispatch(ep, wl.num_experts, wl.top_k, T, inp.num_tokens, inp.hidden, inp.topk_ids,
                            scale=inp.scale, topk_weights=inp.topk_weights,
-                           mask_enabled=wl.enable_rank_mask, active_rank_mask=inp.active_rank_mask)
+                           mask_enabled=wl.enable_rank_mask, active_rank_mask=inp.active_rank_mask,
+                           row_bytes=H * wl.elem_bytes, scale_cols=wl.scale_cols)
     rows = torch.arange(ep * T)
     eo = [bf16_bits(workloads.expert_output_rows(EO_SEED, d, rows, H, special=special))
           for d in range(ep)]

@@ -70,7 +70,11 @@ def test_full_size_sampled(cuda_device, name):
         # 2. sampled tokens as a small oracle problem
         picks = _sample_slots(inp, np.random.default_rng(5))
         Tm = max(1, max(len(v) for v in picks.values()))
-        sub = lambda lst, s: None if lst is None else lst[s][torch.tensor(picks[s], dtype=torch.long)]
+        def sub(lst, s):  # rows of the sampled tokens (fp8 rows indexed as raw bytes)
+            if lst is None:
+                return None
+            x = lst[s].view(torch.uint8) if lst[s].dtype == torch.float8_e4m3fn else lst[s]
+            return x[torch.tensor(picks[s], dtype=torch.long)]
         m_hidden = [sub(inp.hidden, s) for s in range(ep)]
         m_ids = [sub(inp.topk_ids, s) for s in range(ep)]
         m_w = None if inp.topk_weights is None else [sub(inp.topk_weights, s) for s in range(ep)]
@@ -82,7 +86,8 @@ def test_full_size_sampled(cuda_device, name):
             for j, t in enumerate(picks[s]):
                 full_rows[s * Tm + j] = s * T + t
         disp = oracle.dispatch(ep, E, K, Tm, m_counts, m_hidden, m_ids, scale=m_sc, topk_weights=m_w,
-                               mask_enabled=wl.enable_rank_mask, active_rank_mask=inp.active_rank_mask)
+                               mask_enabled=wl.enable_rank_mask, active_rank_mask=inp.active_rank_mask,
+                               row_bytes=H * wl.elem_bytes, scale_cols=wl.scale_cols)
         rows_t = torch.from_numpy(full_rows)
         eo = [bf16_bits(workloads.expert_output_rows(EO_SEED, d, rows_t, H)) for d in range(ep)]
         mout = oracle.combine(ep, E, K, H, Tm, m_counts, m_ids, eo, mask_enabled=wl.enable_rank_mask,
