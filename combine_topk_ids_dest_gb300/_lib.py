@@ -30,7 +30,8 @@ ALL_RANKS = (1 << 64) - 1  # "no mask": every rank active
 # Every symbol include/ep.h declares.
 EXPORTS = ("ep_is_supported", "ep_workspace_size", "ep_create", "ep_create_with_workspace",
            "ep_dispatch", "ep_get_combine_input_buffer", "ep_combine", "ep_destroy",
-           "ep_rank_mask", "ep_last_error")
+           "ep_rank_mask", "ep_last_error", "ep_combine_noalloc")
+EP_NOALLOC_MAX_SLOTS = 65536
 
 
 class EpDispatchResultC(ctypes.Structure):
@@ -89,6 +90,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         L.ep_destroy.restype = i32
         L.ep_rank_mask.argtypes = [ctypes.POINTER(ctypes.c_int), i32]
         L.ep_rank_mask.restype = u64
+        L.ep_combine_noalloc.argtypes = [i32, i32, i32, i32, i32, P, P, u64, P, P, P]
+        L.ep_combine_noalloc.restype = i32
         L.ep_last_error.argtypes = []
         L.ep_last_error.restype = ctypes.c_char_p
         _lib = L

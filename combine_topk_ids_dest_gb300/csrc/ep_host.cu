@@ -243,6 +243,19 @@ ep_status resolve_mask(const ep_handle *h, uint64_t in, uint64_t *out)
 
 }  // namespace
 
+ep_status epk::set_error(ep_status st, const char *fmt, ...)
+{
+    if (st == EP_OK) {
+        g_err[0] = '\0';
+        return st;
+    }
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return st;
+}
+
 extern "C" {
 
 int ep_is_supported(void)

@@ -52,6 +52,10 @@ struct CombineArgs {
     int ep, T, H;
 };
 
+// Records `fmt` as the calling thread's ep_last_error() message (cleared for
+// EP_OK) and returns `st`.
+ep_status set_error(ep_status st, const char *fmt, ...);
+
 // Queue one launch on `stream`; returns the launch's cudaError_t.
 cudaError_t launch_dispatch(const DispatchArgs &a, cudaStream_t stream);
 cudaError_t launch_combine(const CombineArgs &a, cudaStream_t stream);

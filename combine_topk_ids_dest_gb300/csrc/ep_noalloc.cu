@@ -1,0 +1,269 @@
+// ep_noalloc.cu -- ep_combine_noalloc: a combine for callers that cannot
+// allocate device memory.
+//
+// Some callers of this library may not call cudaMalloc (or any allocator)
+// at the point where they combine: code inside a memory arena that owns all
+// device memory after start-up, plug-ins hosted by an inference runtime that
+// forbids allocations of their own, and code between the start and the end
+// of a CUDA stream capture, where allocation calls are illegal. They also
+// may not hold an ep_handle, whose workspace is an allocation. This entry
+// point needs neither: the caller passes the ids, the expert outputs and the
+// result buffers, and the only scratch -- the destination-rank bit set of
+// every slot -- lives in a file-scope __device__ array of fixed size that
+// every GPU loading the library holds until the process exits.
+//
+// Host code never hands that array's name to a kernel (on the host it is a
+// stand-in, not a device address): the first call on each device, with that
+// device current, asks for the array's device address with
+// cudaGetSymbolAddress and caches it; kernels receive that pointer.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "ep_internal.h"
+
+namespace {
+
+constexpr int kNoallocThreads = 128;
+constexpr int kNoallocBatch = 8;
+constexpr int kMaxDevices = 64;
+
+// Routing state of up to EP_NOALLOC_MAX_SLOTS source slots (512 KB).
+static __device__ __align__(256) uint64_t g_noalloc_route[EP_NOALLOC_MAX_SLOTS];
+
+std::mutex g_setup_mu;
+void *g_route_ptr[kMaxDevices] = {nullptr};
+
+struct NoallocArgs {
+    const int32_t *ids[epk::kMaxEp];   // source rank s: [num_tokens[s], top_k]
+    const uint16_t *eo[epk::kMaxEp];   // rank d's bf16 combine input, [ep*T, H]
+    uint16_t *out[epk::kMaxEp];        // source rank s's bf16 output, [num_tokens[s], H]
+    int num_tokens[epk::kMaxEp];
+    uint64_t *route;                   // device address of g_noalloc_route
+    uint64_t active;
+    int ep, num_experts, experts_per_rank, top_k, T, H;
+};
+
+__device__ __forceinline__ uint4 ld_nc16(const void *p)
+{
+    uint4 v;
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+        : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ uint32_t to_bf16x2(float lo, float hi)
+{
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// One thread per slot s*T+t: the set of active ranks owning one of the
+// token's valid expert ids (0 for padding slots). Every slot of the call is
+// written, so nothing left by an earlier call is ever read.
+__global__ void noalloc_route_kernel(const __grid_constant__ NoallocArgs a)
+{
+    const long long n = (long long)a.ep * a.T;
+    for (long long slot = (long long)blockIdx.x * blockDim.x + threadIdx.x; slot < n;
+         slot += (long long)gridDim.x * blockDim.x) {
+        const int s = (int)(slot / a.T);
+        const int t = (int)(slot - (long long)s * a.T);
+        uint64_t m = 0;
+        if (t < a.num_tokens[s]) {
+            const int32_t *row = a.ids[s] + (long long)t * a.top_k;
+            for (int k = 0; k < a.top_k; ++k) {
+                const int e = row[k];
+                if (e >= 0 && e < a.num_experts)
+                    m |= 1ULL << (e / a.experts_per_rank);
+            }
+            m &= a.active;
+        }
+        a.route[slot] = m;
+    }
+}
+
+// One thread per 16-byte column vector of one output row: ascending-rank
+// fp32 sum of the routed rows, one round to bf16.
+__global__ void __launch_bounds__(kNoallocThreads)
+    noalloc_combine_kernel(const __grid_constant__ NoallocArgs a, int blocks_per_row, long long n_blocks)
+{
+    const int nvec = a.H >> 3;
+    for (long long b = blockIdx.x; b < n_blocks; b += gridDim.x) {
+        const long long slot = b / blocks_per_row;
+        const int chunk = (int)(b - slot * blocks_per_row);
+        const int s = (int)(slot / a.T);
+        const int t = (int)(slot - (long long)s * a.T);
+        if (t >= a.num_tokens[s])
+            continue;
+        const int v = chunk * kNoallocThreads + threadIdx.x;
+        if (v >= nvec)
+            continue;
+        uint64_t mm = a.route[slot];
+        const long long off = slot * a.H * 2 + 16 * (long long)v;
+        float acc[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            acc[e] = 0.0f;
+        while (mm) {
+            uint4 x[kNoallocBatch];
+            int nb = 0;
+#pragma unroll
+            for (int j = 0; j < kNoallocBatch; ++j) {
+                if (mm) {
+                    const int d = __ffsll((long long)mm) - 1;
+                    mm &= mm - 1;
+                    x[j] = ld_nc16(reinterpret_cast<const uint8_t *>(a.eo[d]) + off);
+                    nb = j + 1;
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < kNoallocBatch; ++j) {
+                if (j < nb) {
+                    const uint32_t w[4] = {x[j].x, x[j].y, x[j].z, x[j].w};
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        acc[2 * q] = __fadd_rn(acc[2 * q], __uint_as_float(w[q] << 16));
+                        acc[2 * q + 1] = __fadd_rn(acc[2 * q + 1], __uint_as_float(w[q] & 0xffff0000u));
+                    }
+                }
+            }
+        }
+        uint4 o;
+        o.x = to_bf16x2(acc[0], acc[1]);
+        o.y = to_bf16x2(acc[2], acc[3]);
+        o.z = to_bf16x2(acc[4], acc[5]);
+        o.w = to_bf16x2(acc[6], acc[7]);
+        reinterpret_cast<uint4 *>(a.out[s] + (long long)t * a.H)[v] = o;
+    }
+}
+
+bool is_aligned(const void *p, size_t n) { return (reinterpret_cast<uintptr_t>(p) % n) == 0; }
+
+// Device address of g_noalloc_route on the current device, looked up once
+// per device (with that device current) and cached.
+ep_status route_scratch(uint64_t **out)
+{
+    int dev = -1;
+    cudaError_t ce = cudaGetDevice(&dev);
+    if (ce != cudaSuccess)
+        return epk::set_error(EP_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(ce));
+    if (dev < 0 || dev >= kMaxDevices)
+        return epk::set_error(EP_ERR_UNSUPPORTED, "device index %d is beyond %d", dev, kMaxDevices);
+    std::lock_guard<std::mutex> lock(g_setup_mu);
+    if (!g_route_ptr[dev]) {
+        if (!ep_is_supported())
+            return epk::set_error(EP_ERR_UNSUPPORTED, "device %d is not compute capability 10.3", dev);
+        void *p = nullptr;
+        ce = cudaGetSymbolAddress(&p, g_noalloc_route);
+        if (ce != cudaSuccess || !p) {
+            cudaGetLastError();
+            return epk::set_error(EP_ERR_CUDA, "cudaGetSymbolAddress of the routing scratch: %s",
+                                  cudaGetErrorString(ce));
+        }
+        g_route_ptr[dev] = p;
+    }
+    *out = static_cast<uint64_t *>(g_route_ptr[dev]);
+    return EP_OK;
+}
+
+int sm_count_here()
+{
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+        return 152;
+    return n;
+}
+
+}  // namespace
+
+extern "C" ep_status ep_combine_noalloc(int ep_size, int num_experts, int top_k, int hidden,
+                                        int tokens_per_rank, const int32_t *num_tokens,
+                                        const int32_t *const *topk_ids, uint64_t active_rank_mask,
+                                        const void *const *expert_output, void *const *output,
+                                        void *stream)
+{
+    if (ep_size < 1 || ep_size > EP_MAX_EP_SIZE)
+        return epk::set_error(EP_ERR_INVALID_ARG, "ep_size=%d outside [1, %d]", ep_size, EP_MAX_EP_SIZE);
+    if (num_experts < ep_size || num_experts % ep_size)
+        return epk::set_error(EP_ERR_INVALID_ARG, "num_experts=%d is not a positive multiple of ep_size=%d",
+                              num_experts, ep_size);
+    if (top_k < 1 || top_k > EP_MAX_TOP_K)
+        return epk::set_error(EP_ERR_INVALID_ARG, "top_k=%d outside [1, %d]", top_k, EP_MAX_TOP_K);
+    if (hidden < 8 || hidden % 8)
+        return epk::set_error(EP_ERR_INVALID_ARG, "hidden=%d must be a positive multiple of 8", hidden);
+    if (tokens_per_rank < 0)
+        return epk::set_error(EP_ERR_INVALID_ARG, "tokens_per_rank=%d < 0", tokens_per_rank);
+    if ((long long)ep_size * tokens_per_rank > EP_NOALLOC_MAX_SLOTS)
+        return epk::set_error(EP_ERR_INVALID_ARG,
+                              "ep_size*tokens_per_rank=%lld exceeds the %d routing slots of the "
+                              "static scratch of ep_combine_noalloc",
+                              (long long)ep_size * tokens_per_rank, EP_NOALLOC_MAX_SLOTS);
+    if (!num_tokens || !topk_ids || !expert_output || !output)
+        return epk::set_error(EP_ERR_INVALID_ARG,
+                              "num_tokens, topk_ids, expert_output and output must not be NULL");
+    const uint64_t full = ep_size >= 64 ? ~0ULL : ((1ULL << ep_size) - 1);
+    uint64_t mask = active_rank_mask == ~0ULL ? full : active_rank_mask;
+    if (mask & ~full)
+        return epk::set_error(EP_ERR_INVALID_ARG, "active_rank_mask 0x%llx has bits at or above ep_size=%d",
+                              (unsigned long long)mask, ep_size);
+
+    NoallocArgs a;
+    std::memset(&a, 0, sizeof a);
+    for (int d = 0; d < ep_size; ++d) {
+        if (!expert_output[d] || !is_aligned(expert_output[d], 16))
+            return epk::set_error(EP_ERR_INVALID_ARG, "expert_output[%d] is NULL or not 16-byte aligned", d);
+        a.eo[d] = static_cast<const uint16_t *>(expert_output[d]);
+    }
+    for (int s = 0; s < ep_size; ++s) {
+        const int n = num_tokens[s];
+        if (n < 0 || n > tokens_per_rank)
+            return epk::set_error(EP_ERR_INVALID_ARG, "num_tokens[%d]=%d outside [0, tokens_per_rank=%d]", s,
+                                  n, tokens_per_rank);
+        a.num_tokens[s] = n;
+        if (n == 0)
+            continue;
+        if (!topk_ids[s] || !is_aligned(topk_ids[s], 4))
+            return epk::set_error(EP_ERR_INVALID_ARG, "topk_ids[%d] is NULL or not 4-byte aligned", s);
+        if (!output[s] || !is_aligned(output[s], 16))
+            return epk::set_error(EP_ERR_INVALID_ARG, "output[%d] is NULL or not 16-byte aligned", s);
+        a.ids[s] = topk_ids[s];
+        a.out[s] = static_cast<uint16_t *>(output[s]);
+    }
+    uint64_t *route = nullptr;
+    ep_status st = route_scratch(&route);
+    if (st != EP_OK)
+        return st;
+    a.route = route;
+    a.active = mask;
+    a.ep = ep_size;
+    a.num_experts = num_experts;
+    a.experts_per_rank = num_experts / ep_size;
+    a.top_k = top_k;
+    a.T = tokens_per_rank;
+    a.H = hidden;
+
+    const long long n_slots = (long long)ep_size * tokens_per_rank;
+    if (n_slots == 0)
+        return epk::set_error(EP_OK, "");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    long long route_blocks = (n_slots + 255) / 256;
+    const long long cap = (long long)sm_count_here() * 8;
+    if (route_blocks > cap)
+        route_blocks = cap;
+    noalloc_route_kernel<<<(unsigned)route_blocks, 256, 0, s>>>(a);
+    cudaError_t ce = cudaGetLastError();
+    if (ce != cudaSuccess)
+        return epk::set_error(EP_ERR_CUDA, "ep_combine_noalloc routing launch: %s", cudaGetErrorString(ce));
+    const int bpr = (hidden / 8 + kNoallocThreads - 1) / kNoallocThreads;
+    const long long n_blocks = n_slots * bpr;
+    long long grid = n_blocks > (1LL << 30) ? (1LL << 30) : n_blocks;
+    noalloc_combine_kernel<<<(unsigned)grid, kNoallocThreads, 0, s>>>(a, bpr, n_blocks);
+    ce = cudaGetLastError();
+    if (ce != cudaSuccess)
+        return epk::set_error(EP_ERR_CUDA, "ep_combine_noalloc combine launch: %s", cudaGetErrorString(ce));
+    return epk::set_error(EP_OK, "");
+}

@@ -171,6 +171,44 @@ uint64_t ep_rank_mask(const int *ranks, int n);
 /* Message of the calling thread's last failed call ("" if none). */
 const char *ep_last_error(void);
 
+/* Largest ep_size * tokens_per_rank that ep_combine_noalloc accepts. */
+#define EP_NOALLOC_MAX_SLOTS 65536
+
+/* Combine for callers that cannot allocate device memory. The pages have no
+ * counterpart: it exists for code that may not call cudaMalloc or any
+ * allocator where it combines (inside an arena that owns all device memory,
+ * a plug-in of a runtime that forbids its own allocations, or between the
+ * start and end of a stream capture) and that holds no ep_handle, whose
+ * workspace is an allocation.
+ *
+ * It computes what ep_combine computes, from the same ids instead of a
+ * pending dispatch: output[s][t] = bf16( sum over the active ranks d that own
+ * one of topk_ids[s][t]'s valid expert ids, ascending, of expert_output[d]
+ * [s*tokens_per_rank + t] ), fp32 accumulator from +0.0, one
+ * round-to-nearest-even; a token routed nowhere gets +0.0. Results are bit
+ * for bit those of ep_combine after ep_dispatch with the same ids and mask.
+ *  topk_ids[s]      device int32 [num_tokens[s], top_k] (read only)
+ *  num_tokens       host int32 [ep_size], each in [0, tokens_per_rank]
+ *  active_rank_mask bit d = rank d active; UINT64_MAX = all; no bit >= ep_size
+ *  expert_output[d] device bf16 [ep_size*tokens_per_rank, hidden], 16-byte aligned
+ *  output[s]        device bf16 [num_tokens[s], hidden], 16-byte aligned
+ *  stream           cudaStream_t to queue the two kernels on
+ * Scratch: the routing bit set of every slot lives in one file-scope device
+ * array of EP_NOALLOC_MAX_SLOTS entries (512 KB), held by every GPU that
+ * loads the library until the process exits; ep_size * tokens_per_rank
+ * beyond that returns EP_ERR_INVALID_ARG. Each call rewrites every entry it
+ * reads, so nothing needs clearing, but all calls on a device share the
+ * array: calls whose GPU work overlaps (e.g. on two streams) race.
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture. It calls no allocator: no cudaMalloc, no
+ * cudaFree, no allocating library routine. */
+ep_status ep_combine_noalloc(int ep_size, int num_experts, int top_k, int hidden,
+                             int tokens_per_rank, const int32_t *num_tokens,
+                             const int32_t *const *topk_ids, uint64_t active_rank_mask,
+                             const void *const *expert_output, void *const *output,
+                             void *stream);
+
 #ifdef __cplusplus
 }
 #endif
