@@ -2,17 +2,17 @@
 // and state checks, kernel launches.
 //
 // Contract followed (FlashInfer moe_ep pages):
-//  - "flashinfer.moe_ep.MoEEpCommunication", class description: one
-//    in-flight dispatch/combine pair per instance; every dispatch() is
-//    followed by exactly one combine(). dispatch(): runtime_max_tokens_per_rank
-//    is at most max_tokens_per_rank and sets tokens_per_rank (capacity when
-//    absent). get_combine_input_buffer(): valid only between dispatch() and
-//    combine(). destroy(): idempotent.
-//  - "flashinfer.moe_ep.NVLinkOneSidedAlltoAll", dispatch(): active_rank_mask
-//    requires enable_rank_mask; every rank passes topk_weights or none does
-//    (an empty rank passes an empty tensor). combine(): active_rank_mask must
-//    match the dispatch's. get_combine_input_buffer(): an [ep_size *
-//    tokens_per_rank, hidden_size] view of the rank's combine input region.
+//  - "flashinfer.moe_ep.MoEEpCommunication", class description: an instance
+//    alternates dispatch() and combine(), one pair at a time.
+//    dispatch(): runtime_max_tokens_per_rank may not exceed
+//    max_tokens_per_rank and fixes tokens_per_rank (the capacity when not
+//    given). get_combine_input_buffer(): usable from a dispatch() until its
+//    combine(). destroy(): calling it again is harmless.
+//  - "flashinfer.moe_ep.NVLinkOneSidedAlltoAll", dispatch(): a rank mask
+//    needs a handle created with enable_rank_mask; weights come from all
+//    ranks or from none (a rank without tokens sends an empty tensor).
+//    combine(): its mask is the dispatch's. get_combine_input_buffer(): the
+//    rank's combine-input region seen as [ep_size * tokens_per_rank, hidden].
 //
 // Workspace (one device allocation, regions 256-byte aligned, each sized at
 // capacity C = max_tokens_per_rank):
@@ -397,7 +397,7 @@ ep_status ep_get_combine_input_buffer(ep_handle *h, int rank, void **out)
         return fail(EP_ERR_INVALID_ARG, "handle or out is NULL");
     *out = nullptr;
     if (!h->pending)
-        return fail(EP_ERR_STATE, "the combine input buffer is valid only between dispatch and combine");
+        return fail(EP_ERR_STATE, "the combine input buffer exists only from a dispatch until its combine");
     if (rank < 0 || rank >= h->ep)
         return fail(EP_ERR_INVALID_ARG, "rank=%d outside [0, %d)", rank, h->ep);
     *out = h->ws + h->off_comb + (size_t)rank * h->st_comb;

@@ -4,24 +4,23 @@
 // dispatch_kernel (one warp per source slot s*T+t, grid-stride):
 //   routing   -- lane k reads expert id k; the owners' bits are OR-reduced
 //                across the warp (two 32-bit halves for up to 64 ranks) and
-//                ANDed with active_rank_mask ("flashinfer.moe_ep.
-//                NVLinkOneSidedAlltoAll", dispatch(): tokens routed to a
-//                masked-off rank are dropped). The bit set is kept for combine.
+//                ANDed with active_rank_mask (page "flashinfer.moe_ep.
+//                NVLinkOneSidedAlltoAll", dispatch(): a masked-off rank
+//                receives nothing). The bit set is kept for combine.
 //   id plane  -- the slot's id row in every destination rank: the token's ids
 //                where it is routed, invalid_expert_id elsewhere and on padding
 //                slots (same page, class description).
 //   payload   -- the hidden row is read once with 16-byte non-caching loads
 //                and stored to every routed rank's row s*T+t, followed by the
-//                scale and weight rows ("hidden_states, its optional scale
-//                factors, topk_ids and topk_weights travel as payloads of a
-//                single dispatch").
+//                scale and weight rows (same page, class description: one
+//                dispatch carries all four payloads).
 //
 // combine_kernel (one thread per 16-byte column vector of one output row):
 //   reads the row's slot in each routed rank's combine input in ascending
 //   rank order (loads of up to 8 ranks in flight before their adds), adds in
-//   fp32 from +0.0 and rounds once to bf16 ("flashinfer.moe_ep.
-//   MoEEpCommunication", combine(): each token's expert outputs, summed over
-//   ranks).
+//   fp32 from +0.0 and rounds once to bf16 (page "flashinfer.moe_ep.
+//   MoEEpCommunication", combine(): per token, the ranks' expert outputs are
+//   added up).
 //
 // Nothing here is a dense contraction; both kernels are bound by HBM
 // bandwidth, so the design is about coalesced 16-byte accesses and enough

@@ -140,7 +140,7 @@ class EpComm:
                  runtime_max_tokens_per_rank: Optional[int] = None,
                  eplb_local_stats: Optional[Sequence[torch.Tensor]] = None,
                  active_rank_mask=None) -> EpDispatchResult:
-        """Send every rank's tokens to the ranks that own their experts.
+        """Scatter each rank's tokens to the ranks holding one of their top-k experts.
 
         Per rank s: ``hidden_states[s]`` [n_s, hidden] (dtype of the
         communicator), ``topk_ids[s]`` int32 [n_s, top_k], optional
@@ -194,7 +194,7 @@ class EpComm:
     def get_combine_input_buffer(self, dtype: torch.dtype = torch.bfloat16, *, rank: Optional[int] = None):
         """Rank ``rank``'s bf16 [ep_size*tokens_per_rank, hidden] combine input
         (all ranks as a list when ``rank`` is None); None for other dtypes.
-        Valid only between dispatch() and combine()."""
+        Usable from a dispatch() until the combine() that follows it."""
         self._live()
         if dtype != torch.bfloat16:
             return None

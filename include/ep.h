@@ -3,18 +3,18 @@
  * dispatch/combine library (libep_gb300.so).
  *
  * The operation is the one FlashInfer's moe_ep API pages define:
- *  - page "flashinfer.moe_ep.MoEEpCommunication": dispatch() sends each token
- *    to the ranks that own its selected experts; combine() returns each
- *    token's expert outputs summed over ranks; get_combine_input_buffer()
- *    hands out a backend-owned buffer the expert computation may write into;
- *    one dispatch() is followed by exactly one combine(); destroy() is
- *    idempotent.
- *  - page "flashinfer.moe_ep.NVLinkOneSidedAlltoAll": hidden rows, scales,
- *    topk_ids and topk_weights travel as payloads of one dispatch; receive
- *    row source_rank*tokens_per_rank+token holds that token; padding rows and
- *    rows of tokens not routed to a rank get invalid_expert_id routing;
- *    active_rank_mask drops tokens routed to masked-off ranks and must be the
- *    same on dispatch and combine.
+ *  - page "flashinfer.moe_ep.MoEEpCommunication": dispatch() delivers every
+ *    token to each rank that owns one of its top-k experts; combine() adds up,
+ *    per token, what the ranks' experts produced; get_combine_input_buffer()
+ *    lends the expert computation a library-owned output buffer; calls
+ *    alternate dispatch(), combine(), dispatch(), ...; destroy() may be
+ *    repeated.
+ *  - page "flashinfer.moe_ep.NVLinkOneSidedAlltoAll": one dispatch carries
+ *    the hidden row, its scales, the ids and the weights; a receiving rank
+ *    keeps token t of source rank s in row s*tokens_per_rank + t; padding
+ *    slots and tokens the rank does not receive are marked with
+ *    invalid_expert_id; a rank left out of active_rank_mask receives
+ *    nothing, and combine uses the dispatch's mask.
  *
  * All ep_size ranks of the EP group are virtual ranks on ONE GPU: every
  * rank's inputs, receive buffers and combine inputs live in that GPU's
@@ -141,7 +141,7 @@ ep_status ep_dispatch(ep_handle *h, const void *const *hidden, const float *cons
 
 /* Device pointer to rank `rank`'s backend-owned combine input: bf16
  * [ep_size*tokens_per_rank, hidden] of the pending dispatch. Passing it (or
- * NULL) to ep_combine saves a copy. Valid between ep_dispatch and
+ * NULL) to ep_combine avoids one copy. Valid between ep_dispatch and
  * ep_combine; EP_ERR_STATE outside (MoEEpCommunication.get_combine_input_buffer,
  * NVLinkOneSidedAlltoAll.get_combine_input_buffer). */
 ep_status ep_get_combine_input_buffer(ep_handle *h, int rank, void **out);

@@ -7,19 +7,20 @@
  * calls it, and this file includes nothing of the CUDA library.
  *
  * What it follows (FlashInfer moe_ep API pages):
- *  - "flashinfer.moe_ep.MoEEpCommunication", dispatch(): each token goes to
- *    the ranks that own its selected experts; combine(): each token's expert
- *    outputs, summed over ranks; expert_output is [ep_size*tokens_per_rank,
- *    hidden]; runtime_max_tokens_per_rank sets tokens_per_rank (capacity when
- *    absent).
- *  - "flashinfer.moe_ep.NVLinkOneSidedAlltoAll", class description: hidden
- *    rows, scales, topk_ids and topk_weights travel as payloads of one
- *    dispatch; row source_rank*tokens_per_rank+token holds that token; rows
- *    past a source rank's token count and rows of tokens not routed here get
- *    invalid_expert_id routing. dispatch(): tokens routed to a rank that
- *    active_rank_mask leaves out are dropped.
- *  - "flashinfer.moe_ep.CakeAlltoAll", class description: the same padding
- *    rule.
+ *  - "flashinfer.moe_ep.MoEEpCommunication", dispatch(): a token is delivered
+ *    to every rank owning one of its top-k experts; combine(): per token, the
+ *    ranks' expert outputs are added up; the combine input has one row per
+ *    (source rank, slot), ep_size*tokens_per_rank rows of `hidden`;
+ *    runtime_max_tokens_per_rank fixes tokens_per_rank, the capacity
+ *    standing in when it is not given.
+ *  - "flashinfer.moe_ep.NVLinkOneSidedAlltoAll", class description: one
+ *    dispatch carries the hidden row, its scales, the ids and the weights;
+ *    a receiving rank keeps token t of source rank s in row
+ *    s*tokens_per_rank + t; slots past a source's token count, and tokens
+ *    the rank does not receive, are marked with invalid_expert_id.
+ *    dispatch(): a rank left out of active_rank_mask receives nothing.
+ *  - "flashinfer.moe_ep.CakeAlltoAll", class description: padding slots are
+ *    marked the same way.
  *
  * Readings where the pages say nothing (each also fixed by a test):
  *  - invalid_expert_id is -1; ids are int32; weights and scales are fp32.
