@@ -30,11 +30,39 @@
 namespace epk {
 namespace {
 
+// Launch shapes (compile-time; -D overrides exist for tuning sweeps).
+#ifndef EP_DISPATCH_THREADS
+#define EP_DISPATCH_THREADS 256
+#endif
+#ifndef EP_DISPATCH_VEC_PER_LANE
+#define EP_DISPATCH_VEC_PER_LANE 16
+#endif
+#ifndef EP_DISPATCH_BLOCKS_PER_SM
+#define EP_DISPATCH_BLOCKS_PER_SM 64
+#endif
+#ifndef EP_COMBINE_MAX_THREADS
+#define EP_COMBINE_MAX_THREADS 256
+#endif
+#ifndef EP_COMBINE_VPT
+#define EP_COMBINE_VPT 4  // 16-byte column vectors per combine thread
+#endif
+#ifndef EP_DISPATCH_STORE_HINT
+#define EP_DISPATCH_STORE_HINT 0  // 0 plain, 1 .cs (evict-first), 2 .L1::no_allocate
+#endif
+#ifndef EP_COMBINE_L2_PREFETCH
+#define EP_COMBINE_L2_PREFETCH 0  // 1: .L2::256B on the combine's row loads
+#endif
+
 constexpr unsigned kFull = 0xffffffffu;
-constexpr int kDispatchThreads = 256;  // 8 warps, one slot each
-constexpr int kDispatchVecPerLane = 8;  // 16-byte vectors per lane per chunk (4 KB per warp)
-constexpr int kCombineThreads = 128;
-constexpr int kCombineBatch = 8;  // rank rows loaded before their adds
+constexpr int kDispatchThreads = EP_DISPATCH_THREADS;  // one warp per slot
+constexpr int kDispatchVecPerLane = EP_DISPATCH_VEC_PER_LANE;  // 16-byte vectors per lane per chunk
+constexpr int kDispatchBlocksPerSm = EP_DISPATCH_BLOCKS_PER_SM;  // grid cap, in blocks per SM
+constexpr int kCombineMaxThreads = EP_COMBINE_MAX_THREADS;
+constexpr int kCombineVpt = EP_COMBINE_VPT;
+#ifndef EP_COMBINE_BATCH
+#define EP_COMBINE_BATCH 2
+#endif
+constexpr int kCombineBatch = EP_COMBINE_BATCH;  // rank rows loaded before their adds
 
 __device__ __forceinline__ uint4 ld_stream(const void *p)
 {
@@ -43,6 +71,34 @@ __device__ __forceinline__ uint4 ld_stream(const void *p)
         : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
         : "l"(p));
     return v;
+}
+
+__device__ __forceinline__ uint4 ld_rows(const void *p)
+{
+#if EP_COMBINE_L2_PREFETCH
+    uint4 v;
+    asm("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
+        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+        : "l"(p));
+    return v;
+#else
+    return ld_stream(p);
+#endif
+}
+
+__device__ __forceinline__ void st_row(uint4 *p, const uint4 &v)
+{
+#if EP_DISPATCH_STORE_HINT == 1
+    asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w)
+                 : "memory");
+#elif EP_DISPATCH_STORE_HINT == 2
+    asm volatile("st.global.L1::no_allocate.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w)
+                 : "memory");
+#else
+    *p = v;
+#endif
 }
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -148,7 +204,7 @@ __global__ void __launch_bounds__(kDispatchThreads)
                 for (int j = 0; j < kDispatchVecPerLane; ++j) {
                     const int idx = c0 + j * 32 + lane;
                     if (idx < nvec)
-                        dst[idx] = v[j];
+                        st_row(dst + idx, v[j]);
                 }
             }
         }
@@ -176,10 +232,11 @@ __global__ void __launch_bounds__(kDispatchThreads)
     }
 }
 
-__global__ void __launch_bounds__(kCombineThreads)
+__global__ void __launch_bounds__(kCombineMaxThreads)
     combine_kernel(const __grid_constant__ CombineArgs a, int blocks_per_row, long long n_blocks)
 {
     const int nvec = a.H >> 3;  // 8 bf16 per 16-byte vector
+    const int nthr = blockDim.x;
     for (long long b = blockIdx.x; b < n_blocks; b += gridDim.x) {
         const long long slot = b / blocks_per_row;
         const int chunk = (int)(b - slot * blocks_per_row);
@@ -187,51 +244,83 @@ __global__ void __launch_bounds__(kCombineThreads)
         const int t = (int)(slot - (long long)s * a.T);
         if (t >= a.num_tokens[s])
             continue;  // block-uniform
-        const int v = chunk * kCombineThreads + threadIdx.x;
-        if (v >= nvec)
+        const int v0 = chunk * (nthr * kCombineVpt) + threadIdx.x;
+        if (v0 >= nvec)
             continue;
         const uint64_t m = a.route_mask[slot];
-        const long long off = (slot * a.H) * 2 + 16 * (long long)v;  // byte offset in a rank's buffer
+        const long long row = (slot * a.H) * 2;  // byte offset of the slot's row in a rank's buffer
 
-        float acc[8];
+        float acc[kCombineVpt][8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e)
-            acc[e] = 0.0f;
+        for (int j = 0; j < kCombineVpt; ++j)
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                acc[j][e] = 0.0f;
 
         uint64_t mm = m;
         while (mm) {
-            uint4 x[kCombineBatch];
+            uint4 x[kCombineBatch][kCombineVpt];
             int nb = 0;
 #pragma unroll
-            for (int j = 0; j < kCombineBatch; ++j) {
+            for (int r = 0; r < kCombineBatch; ++r) {
                 if (mm) {
                     const int d = __ffsll((long long)mm) - 1;
                     mm &= mm - 1;
-                    x[j] = ld_stream(reinterpret_cast<const uint8_t *>(a.eo[d]) + off);
-                    nb = j + 1;
+                    const uint8_t *base = reinterpret_cast<const uint8_t *>(a.eo[d]) + row;
+#pragma unroll
+                    for (int j = 0; j < kCombineVpt; ++j) {
+                        const int v = v0 + j * nthr;
+                        if (v < nvec)
+                            x[r][j] = ld_rows(base + 16 * (long long)v);
+                    }
+                    nb = r + 1;
                 }
             }
 #pragma unroll
-            for (int j = 0; j < kCombineBatch; ++j) {
-                if (j < nb) {
-                    acc[0] = __fadd_rn(acc[0], bf16_lo(x[j].x));
-                    acc[1] = __fadd_rn(acc[1], bf16_hi(x[j].x));
-                    acc[2] = __fadd_rn(acc[2], bf16_lo(x[j].y));
-                    acc[3] = __fadd_rn(acc[3], bf16_hi(x[j].y));
-                    acc[4] = __fadd_rn(acc[4], bf16_lo(x[j].z));
-                    acc[5] = __fadd_rn(acc[5], bf16_hi(x[j].z));
-                    acc[6] = __fadd_rn(acc[6], bf16_lo(x[j].w));
-                    acc[7] = __fadd_rn(acc[7], bf16_hi(x[j].w));
+            for (int r = 0; r < kCombineBatch; ++r) {
+                if (r < nb) {
+#pragma unroll
+                    for (int j = 0; j < kCombineVpt; ++j) {
+                        acc[j][0] = __fadd_rn(acc[j][0], bf16_lo(x[r][j].x));
+                        acc[j][1] = __fadd_rn(acc[j][1], bf16_hi(x[r][j].x));
+                        acc[j][2] = __fadd_rn(acc[j][2], bf16_lo(x[r][j].y));
+                        acc[j][3] = __fadd_rn(acc[j][3], bf16_hi(x[r][j].y));
+                        acc[j][4] = __fadd_rn(acc[j][4], bf16_lo(x[r][j].z));
+                        acc[j][5] = __fadd_rn(acc[j][5], bf16_hi(x[r][j].z));
+                        acc[j][6] = __fadd_rn(acc[j][6], bf16_lo(x[r][j].w));
+                        acc[j][7] = __fadd_rn(acc[j][7], bf16_hi(x[r][j].w));
+                    }
                 }
             }
         }
-        uint4 o;
-        o.x = pack_bf16x2(acc[0], acc[1]);
-        o.y = pack_bf16x2(acc[2], acc[3]);
-        o.z = pack_bf16x2(acc[4], acc[5]);
-        o.w = pack_bf16x2(acc[6], acc[7]);
-        reinterpret_cast<uint4 *>(a.out[s] + (long long)t * a.H)[v] = o;
+        uint4 *out = reinterpret_cast<uint4 *>(a.out[s] + (long long)t * a.H);
+#pragma unroll
+        for (int j = 0; j < kCombineVpt; ++j) {
+            const int v = v0 + j * nthr;
+            if (v < nvec) {
+                uint4 o;
+                o.x = pack_bf16x2(acc[j][0], acc[j][1]);
+                o.y = pack_bf16x2(acc[j][2], acc[j][3]);
+                o.z = pack_bf16x2(acc[j][4], acc[j][5]);
+                o.w = pack_bf16x2(acc[j][6], acc[j][7]);
+                out[v] = o;
+            }
+        }
     }
+}
+
+// Block width of the combine: the row's vectors are split into chunks of
+// threads*VPT; a width whose chunks tile the row exactly leaves no idle
+// threads (64 for 4096-wide rows, 32 for 7168-wide rows). Preference order
+// from measurements on GB300.
+int combine_threads(int nvec)
+{
+    const int per_thread = kCombineVpt;
+    const int candidates[] = {64, 32, 128};
+    for (int c : candidates)
+        if (c <= kCombineMaxThreads && nvec % (c * per_thread) == 0)
+            return c;
+    return 64;
 }
 
 int sm_count()
@@ -258,7 +347,7 @@ cudaError_t launch_dispatch(const DispatchArgs &a, cudaStream_t stream)
         return cudaSuccess;
     const int wpb = kDispatchThreads / 32;
     long long blocks = (n_slots + wpb - 1) / wpb;
-    const long long cap = (long long)sm_count() * 8;  // 8 resident blocks of 256 per SM
+    const long long cap = (long long)sm_count() * kDispatchBlocksPerSm;
     if (blocks > cap)
         blocks = cap;
     dispatch_kernel<<<(unsigned)blocks, kDispatchThreads, 0, stream>>>(a);
@@ -268,14 +357,16 @@ cudaError_t launch_dispatch(const DispatchArgs &a, cudaStream_t stream)
 cudaError_t launch_combine(const CombineArgs &a, cudaStream_t stream)
 {
     const int nvec = a.H >> 3;
-    const int bpr = (nvec + kCombineThreads - 1) / kCombineThreads;
+    const int threads = combine_threads(nvec);
+    const int per_block = threads * kCombineVpt;
+    const int bpr = (nvec + per_block - 1) / per_block;
     const long long n_blocks = (long long)a.ep * a.T * bpr;
     if (n_blocks == 0)
         return cudaSuccess;
     long long grid = n_blocks;
     if (grid > (1LL << 30))
         grid = 1LL << 30;
-    combine_kernel<<<(unsigned)grid, kCombineThreads, 0, stream>>>(a, bpr, n_blocks);
+    combine_kernel<<<(unsigned)grid, threads, 0, stream>>>(a, bpr, n_blocks);
     return cudaGetLastError();
 }
 
