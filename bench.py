@@ -4,9 +4,10 @@
 A step (a "round") is one ep_dispatch then one ep_combine of a whole EP group
 of virtual ranks, on one stream, with the inputs resident in HBM. The
 combine reads the backend combine-input buffers, filled once (untimed) with
-stand-in expert outputs. L2 is flushed (a 256 MB write) before each timed
-step, outside the step's CUDA events; the workloads' per-round traffic is
-also far larger than L2.
+stand-in expert outputs. L2 is flushed before each timed step, outside the
+step's CUDA events (a 256 MB buffer written, then read back so the flush
+leaves no dirty lines behind); the prefill workload's traffic is also far
+larger than L2.
 
 Metric: algorithmic bytes per round / round time, in GB/s, and that as a
 fraction of the measured HBM copy bandwidth. Algorithmic bytes per round,
@@ -111,6 +112,22 @@ def recorded_traffic(kernel: str, workload: str):
         if m and m.group(1) == kernel and m.group(2) == workload and m.group(4) == src:
             return int(m.group(3))
     return None
+
+
+class L2Flush:
+    """Evicts L2 between timed steps: writes a 256 MB buffer (twice L2), and in
+    "write+read" mode then reads it back, so that L2 holds clean lines and the
+    next timed kernel does not pay for writing back the flush's dirty data."""
+
+    def __init__(self, device, mode="write+read"):
+        self.mode = mode
+        self.buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+        self.sink = torch.empty((), dtype=torch.int64, device=device)
+
+    def __call__(self, i):
+        self.buf.fill_(i & 0xFF)
+        if self.mode == "write+read":
+            torch.sum(self.buf.view(torch.int64), dim=0, out=self.sink)
 
 
 class _Null:
@@ -294,8 +311,8 @@ def workload_config(wl, b):
             "max_tokens_per_rank": wl.capacity, "tokens_per_rank": wl.tokens_per_rank,
             "ids": wl.ids, "rank_mask_drops": list(wl.dropped_ranks) if wl.dropped_ranks else None,
             "tokens": b["N"], "routed_pairs": b["P"], "bytes_per_round": b["total"],
-            "l2": "inputs larger than L2 and L2 flushed (256 MB write) before each timed step, "
-                  "outside its events",
+            "l2": "L2 flushed before each timed step, outside its events: 256 MB written then read "
+                  "back (clean, cold L2); the prefill inputs are also larger than L2",
             "combine_input": "backend buffer, filled once with stand-in expert outputs (untimed)"}
 
 
@@ -311,7 +328,7 @@ def run_ours(args, rank, world):
     wl = workloads.WORKLOADS[args.workload]
     inp = workloads.make_inputs(wl)
     b = round_bytes(inp)
-    dtype = torch.bfloat16 if wl.dtype == "bf16" else torch.float8_e4m3fn
+    dtype = wl.torch_dtype
     comm = EpComm(wl.ep_size, wl.num_experts, wl.top_k, wl.hidden, wl.capacity, dtype=dtype,
                   enable_rank_mask=wl.enable_rank_mask, device=dev)
     mask = inp.active_rank_mask if wl.enable_rank_mask else None
@@ -320,7 +337,7 @@ def run_ours(args, rank, world):
     wts = None if inp.topk_weights is None else [x.to(dev) for x in inp.topk_weights]
     scl = None if inp.scale is None else [x.to(dev) for x in inp.scale]
     out = [torch.empty(n, wl.hidden, dtype=torch.bfloat16, device=dev) for n in inp.num_tokens]
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev, args.l2_flush)
 
     def dispatch():
         return comm.dispatch(hid, ids, wts, hidden_states_scale=scl,
@@ -349,7 +366,7 @@ def run_ours(args, rank, world):
 
     def timed_rounds(run_dispatch, run_combine, steps, warmup, clocks=None):
         for i in range(warmup):
-            flush.fill_(i & 0xFF)
+            flush(i)
             run_dispatch()
             run_combine()
         torch.cuda.synchronize(dev)
@@ -359,7 +376,7 @@ def run_ours(args, rank, world):
         with (clocks if clocks is not None else _Null()):
             torch.cuda.synchronize(dev)
             for i in range(steps):
-                flush.fill_((i + 1) & 0xFF)
+                flush(i + 1)
                 ev[i][0].record()
                 run_dispatch()
                 ev[i][1].record()
@@ -422,6 +439,12 @@ def run_ours(args, rank, world):
         "gpu_launches": launches_per_round * args.steps,
         "clocks": clocks.summary(),
     }
+    l2 = {"write": "L2 flushed before each timed step, outside its events: 256 MB written",
+          "write+read": "L2 flushed before each timed step, outside its events: 256 MB written then "
+                        "read back (clean, cold L2)"}[args.l2_flush]
+    if b["total"] > (128 << 20):
+        l2 += "; per-round traffic larger than L2"
+    line["config"]["l2"] = l2
     if world == 1 and not args.no_cpu_baseline:
         s, eo, sb, desc = oracle_sample(inp, args.cpu_seconds)
         t0 = time.perf_counter()
@@ -519,6 +542,8 @@ def main():
     ap.add_argument("--reference-seconds", type=float, default=120.0,
                     help="total oracle time of the reference arm")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--l2-flush", default="write+read", choices=["write", "write+read"],
+                    help="how L2 is evicted between timed steps")
     ap.add_argument("--tokens-per-rank", type=int, default=None,
                     help="shrink the workload to this many tokens per rank (profiling runs only)")
     args = ap.parse_args()

@@ -21,6 +21,9 @@ STATUS_NAMES = {0: "EP_OK", 1: "EP_ERR_INVALID_ARG", 2: "EP_ERR_STATE", 3: "EP_E
 
 EP_DTYPE_BF16 = 0
 EP_DTYPE_FP8_E4M3 = 1
+EP_DTYPE_FP16 = 2
+EP_DTYPE_FP32 = 3
+EP_SCALE_COLS_DEFAULT = -1
 EP_INVALID_EXPERT_ID = -1
 EP_MAX_EP_SIZE = 64
 EP_MAX_TOP_K = 32
@@ -30,7 +33,8 @@ ALL_RANKS = (1 << 64) - 1  # "no mask": every rank active
 # Every symbol include/ep.h declares.
 EXPORTS = ("ep_is_supported", "ep_workspace_size", "ep_create", "ep_create_with_workspace",
            "ep_dispatch", "ep_get_combine_input_buffer", "ep_combine", "ep_destroy",
-           "ep_rank_mask", "ep_last_error", "ep_combine_noalloc")
+           "ep_rank_mask", "ep_last_error", "ep_combine_noalloc", "ep_workspace_size_ex",
+           "ep_create_ex", "ep_dispatch_ex")
 EP_NOALLOC_MAX_SLOTS = 65536
 
 
@@ -40,7 +44,24 @@ class EpDispatchResultC(ctypes.Structure):
                 ("recv_hidden", ctypes.POINTER(ctypes.c_void_p)),
                 ("recv_scale", ctypes.POINTER(ctypes.c_void_p)),
                 ("recv_topk_ids", ctypes.POINTER(ctypes.c_void_p)),
-                ("recv_topk_weights", ctypes.POINTER(ctypes.c_void_p))]
+                ("recv_topk_weights", ctypes.POINTER(ctypes.c_void_p)),
+                ("eplb_global_stats", ctypes.c_void_p),
+                ("eplb_stats_bytes", ctypes.c_int)]
+
+
+class EpConfigC(ctypes.Structure):
+    _fields_ = [("ep_size", ctypes.c_int), ("num_experts", ctypes.c_int), ("top_k", ctypes.c_int),
+                ("hidden", ctypes.c_int), ("max_tokens_per_rank", ctypes.c_int), ("dtype", ctypes.c_int),
+                ("enable_rank_mask", ctypes.c_int), ("scale_cols", ctypes.c_int),
+                ("eplb_stats_max_bytes", ctypes.c_int)]
+
+
+class EpDispatchArgsC(ctypes.Structure):
+    _fields_ = [("hidden", ctypes.c_void_p), ("hidden_scale", ctypes.c_void_p),
+                ("topk_ids", ctypes.c_void_p), ("topk_weights", ctypes.c_void_p),
+                ("num_tokens", ctypes.c_void_p), ("runtime_max_tokens_per_rank", ctypes.c_int),
+                ("active_rank_mask", ctypes.c_uint64), ("eplb_local_stats", ctypes.c_void_p),
+                ("eplb_stats_bytes", ctypes.c_int)]
 
 
 class EpError(RuntimeError):
@@ -90,6 +111,13 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         L.ep_destroy.restype = i32
         L.ep_rank_mask.argtypes = [ctypes.POINTER(ctypes.c_int), i32]
         L.ep_rank_mask.restype = u64
+        L.ep_workspace_size_ex.argtypes = [ctypes.POINTER(EpConfigC), ctypes.POINTER(sz)]
+        L.ep_workspace_size_ex.restype = i32
+        L.ep_create_ex.argtypes = [ctypes.POINTER(EpConfigC), P, sz, PP]
+        L.ep_create_ex.restype = i32
+        L.ep_dispatch_ex.argtypes = [P, ctypes.POINTER(EpDispatchArgsC), P,
+                                     ctypes.POINTER(EpDispatchResultC)]
+        L.ep_dispatch_ex.restype = i32
         L.ep_combine_noalloc.argtypes = [i32, i32, i32, i32, i32, P, P, u64, P, P, P]
         L.ep_combine_noalloc.restype = i32
         L.ep_last_error.argtypes = []

@@ -17,11 +17,12 @@
 // Workspace (one device allocation, regions 256-byte aligned, each sized at
 // capacity C = max_tokens_per_rank):
 //   recv_hidden  [ep][ep*C][row_bytes]
-//   recv_scale   [ep][ep*C][H/128] fp32     (when H % 128 == 0)
+//   recv_scale   [ep][ep*C][scale_cols] fp32  (scale_cols = H/128 by default)
 //   recv_ids     [ep][ep*C][K] int32
 //   recv_weights [ep][ep*C][K] fp32
 //   combine_in   [ep][ep*C][H] bf16
 //   route_mask   [ep*C] uint64
+//   eplb_stats   [ep][eplb_stats_max_bytes]  (the gathered eplb_local_stats)
 // A step with tokens_per_rank T uses the first ep*T rows of each region, so
 // receive row s*T+t of rank d sits at region base + d*stride + (s*T+t)*row.
 #include <cstdarg>
@@ -37,12 +38,13 @@ struct ep_handle {
     ep_dtype dtype;
     int elem_bytes, row_bytes, scale_cols;
     int mask_enabled;
+    int eplb_max_bytes;
     int device;
 
     uint8_t *ws;
     size_t ws_bytes;
     bool owns_ws;
-    size_t off_hidden, off_scale, off_ids, off_weights, off_comb, off_mask;
+    size_t off_hidden, off_scale, off_ids, off_weights, off_comb, off_mask, off_eplb;
     size_t st_hidden, st_scale, st_ids, st_weights, st_comb;  // bytes per rank region
 
     // state of the pending dispatch
@@ -84,30 +86,73 @@ uint64_t full_mask(int ep) { return ep >= 64 ? ~0ULL : ((1ULL << ep) - 1); }
 
 struct Layout {
     int elem_bytes, row_bytes, scale_cols;
-    size_t off_hidden, off_scale, off_ids, off_weights, off_comb, off_mask, total;
+    size_t off_hidden, off_scale, off_ids, off_weights, off_comb, off_mask, off_eplb, total;
     size_t st_hidden, st_scale, st_ids, st_weights, st_comb;
 };
 
-ep_status plan(int ep, int E, int K, int H, int C, ep_dtype dtype, Layout *L)
+int dtype_bytes(ep_dtype dtype)
 {
+    switch (dtype) {
+    case EP_DTYPE_BF16:
+    case EP_DTYPE_FP16:
+        return 2;
+    case EP_DTYPE_FP8_E4M3:
+        return 1;
+    case EP_DTYPE_FP32:
+        return 4;
+    }
+    return 0;
+}
+
+ep_config default_config(int ep, int E, int K, int H, int C, ep_dtype dtype, int enable_rank_mask)
+{
+    ep_config c;
+    c.ep_size = ep;
+    c.num_experts = E;
+    c.top_k = K;
+    c.hidden = H;
+    c.max_tokens_per_rank = C;
+    c.dtype = dtype;
+    c.enable_rank_mask = enable_rank_mask;
+    c.scale_cols = EP_SCALE_COLS_DEFAULT;
+    c.eplb_stats_max_bytes = 0;
+    return c;
+}
+
+ep_status plan(const ep_config *cfg, Layout *L)
+{
+    if (!cfg)
+        return fail(EP_ERR_INVALID_ARG, "config is NULL");
+    const int ep = cfg->ep_size, E = cfg->num_experts, K = cfg->top_k, H = cfg->hidden;
+    const int C = cfg->max_tokens_per_rank;
+    const ep_dtype dtype = cfg->dtype;
     if (ep < 1 || ep > EP_MAX_EP_SIZE)
         return fail(EP_ERR_INVALID_ARG, "ep_size=%d outside [1, %d]", ep, EP_MAX_EP_SIZE);
     if (E < ep || E % ep != 0)
         return fail(EP_ERR_INVALID_ARG, "num_experts=%d is not a positive multiple of ep_size=%d", E, ep);
     if (K < 1 || K > EP_MAX_TOP_K)
         return fail(EP_ERR_INVALID_ARG, "top_k=%d outside [1, %d]", K, EP_MAX_TOP_K);
-    if (dtype != EP_DTYPE_BF16 && dtype != EP_DTYPE_FP8_E4M3)
+    const int elem = dtype_bytes(dtype);
+    if (elem == 0)
         return fail(EP_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
-    const int elem = dtype == EP_DTYPE_BF16 ? 2 : 1;
     if (H < 1 || ((long long)H * elem) % 16 != 0)
         return fail(EP_ERR_INVALID_ARG, "hidden=%d: a row must be a positive multiple of 16 bytes", H);
     if (H % 8 != 0)
         return fail(EP_ERR_INVALID_ARG, "hidden=%d: the bf16 combine rows need hidden %% 8 == 0", H);
     if (C < 0)
         return fail(EP_ERR_INVALID_ARG, "max_tokens_per_rank=%d < 0", C);
+    if (cfg->scale_cols < EP_SCALE_COLS_DEFAULT)
+        return fail(EP_ERR_INVALID_ARG, "scale_cols=%d: use -1 (default), 0 or a positive count",
+                    cfg->scale_cols);
+    if (cfg->eplb_stats_max_bytes < 0 || cfg->eplb_stats_max_bytes % 4 != 0)
+        return fail(EP_ERR_INVALID_ARG, "eplb_stats_max_bytes=%d must be a non-negative multiple of 4",
+                    cfg->eplb_stats_max_bytes);
     L->elem_bytes = elem;
     L->row_bytes = H * elem;
-    L->scale_cols = (H % EP_SCALE_GROUP == 0) ? H / EP_SCALE_GROUP : 0;
+    if (cfg->scale_cols == EP_SCALE_COLS_DEFAULT)
+        L->scale_cols = (H % EP_SCALE_GROUP == 0) ? H / EP_SCALE_GROUP : 0;
+    else
+        L->scale_cols = cfg->scale_cols;
     const size_t rows = (size_t)ep * (size_t)C;
     L->st_hidden = align256(rows * L->row_bytes);
     L->st_scale = align256(rows * L->scale_cols * sizeof(float));
@@ -127,20 +172,23 @@ ep_status plan(int ep, int E, int K, int H, int C, ep_dtype dtype, Layout *L)
     off += L->st_comb * ep;
     L->off_mask = off;
     off += align256(rows * sizeof(uint64_t));
+    L->off_eplb = off;
+    off += align256((size_t)ep * (size_t)cfg->eplb_stats_max_bytes);
     L->total = off < 256 ? 256 : off;
     return EP_OK;
 }
 
-ep_status make_handle(int ep, int E, int K, int H, int C, ep_dtype dtype, int enable_rank_mask,
-                      void *ws, size_t ws_bytes, bool own, ep_handle **out)
+ep_status make_handle(const ep_config *cfg, void *ws, size_t ws_bytes, bool own, ep_handle **out)
 {
     if (!out)
         return fail(EP_ERR_INVALID_ARG, "out is NULL");
     *out = nullptr;
     Layout L;
-    ep_status st = plan(ep, E, K, H, C, dtype, &L);
+    ep_status st = plan(cfg, &L);
     if (st != EP_OK)
         return st;
+    const int ep = cfg->ep_size, E = cfg->num_experts, K = cfg->top_k, H = cfg->hidden;
+    const int C = cfg->max_tokens_per_rank;
     int dev = 0;
     cudaError_t ce = cudaGetDevice(&dev);
     if (ce != cudaSuccess)
@@ -175,11 +223,12 @@ ep_status make_handle(int ep, int E, int K, int H, int C, ep_dtype dtype, int en
     h->hidden = H;
     h->capacity = C;
     h->experts_per_rank = E / ep;
-    h->dtype = dtype;
+    h->dtype = cfg->dtype;
     h->elem_bytes = L.elem_bytes;
     h->row_bytes = L.row_bytes;
     h->scale_cols = L.scale_cols;
-    h->mask_enabled = enable_rank_mask ? 1 : 0;
+    h->mask_enabled = cfg->enable_rank_mask ? 1 : 0;
+    h->eplb_max_bytes = cfg->eplb_stats_max_bytes;
     h->device = dev;
     h->ws = static_cast<uint8_t *>(ws);
     h->ws_bytes = ws_bytes;
@@ -190,6 +239,7 @@ ep_status make_handle(int ep, int E, int K, int H, int C, ep_dtype dtype, int en
     h->off_weights = L.off_weights;
     h->off_comb = L.off_comb;
     h->off_mask = L.off_mask;
+    h->off_eplb = L.off_eplb;
     h->st_hidden = L.st_hidden;
     h->st_scale = L.st_scale;
     h->st_ids = L.st_ids;
@@ -277,10 +327,16 @@ int ep_is_supported(void)
 ep_status ep_workspace_size(int ep_size, int num_experts, int top_k, int hidden,
                             int max_tokens_per_rank, ep_dtype dtype, size_t *bytes)
 {
+    const ep_config cfg = default_config(ep_size, num_experts, top_k, hidden, max_tokens_per_rank, dtype, 0);
+    return ep_workspace_size_ex(&cfg, bytes);
+}
+
+ep_status ep_workspace_size_ex(const ep_config *cfg, size_t *bytes)
+{
     if (!bytes)
         return fail(EP_ERR_INVALID_ARG, "bytes is NULL");
     Layout L;
-    ep_status st = plan(ep_size, num_experts, top_k, hidden, max_tokens_per_rank, dtype, &L);
+    ep_status st = plan(cfg, &L);
     if (st != EP_OK)
         return st;
     *bytes = L.total;
@@ -290,16 +346,23 @@ ep_status ep_workspace_size(int ep_size, int num_experts, int top_k, int hidden,
 ep_status ep_create(int ep_size, int num_experts, int top_k, int hidden, int max_tokens_per_rank,
                     ep_dtype dtype, int enable_rank_mask, ep_handle **out)
 {
-    return make_handle(ep_size, num_experts, top_k, hidden, max_tokens_per_rank, dtype,
-                       enable_rank_mask, nullptr, 0, true, out);
+    const ep_config cfg = default_config(ep_size, num_experts, top_k, hidden, max_tokens_per_rank, dtype,
+                                         enable_rank_mask);
+    return make_handle(&cfg, nullptr, 0, true, out);
 }
 
 ep_status ep_create_with_workspace(int ep_size, int num_experts, int top_k, int hidden,
                                    int max_tokens_per_rank, ep_dtype dtype, int enable_rank_mask,
                                    void *workspace, size_t bytes, ep_handle **out)
 {
-    return make_handle(ep_size, num_experts, top_k, hidden, max_tokens_per_rank, dtype,
-                       enable_rank_mask, workspace, bytes, false, out);
+    const ep_config cfg = default_config(ep_size, num_experts, top_k, hidden, max_tokens_per_rank, dtype,
+                                         enable_rank_mask);
+    return make_handle(&cfg, workspace, bytes, false, out);
+}
+
+ep_status ep_create_ex(const ep_config *cfg, void *workspace, size_t bytes, ep_handle **out)
+{
+    return make_handle(cfg, workspace, bytes, workspace == nullptr, out);
 }
 
 ep_status ep_dispatch(ep_handle *h, const void *const *hidden, const float *const *hidden_scale,
@@ -307,10 +370,33 @@ ep_status ep_dispatch(ep_handle *h, const void *const *hidden, const float *cons
                       const int32_t *num_tokens, int runtime_max_tokens_per_rank,
                       uint64_t active_rank_mask, void *stream, ep_dispatch_result *out)
 {
+    ep_dispatch_args args;
+    args.hidden = hidden;
+    args.hidden_scale = hidden_scale;
+    args.topk_ids = topk_ids;
+    args.topk_weights = topk_weights;
+    args.num_tokens = num_tokens;
+    args.runtime_max_tokens_per_rank = runtime_max_tokens_per_rank;
+    args.active_rank_mask = active_rank_mask;
+    args.eplb_local_stats = nullptr;
+    args.eplb_stats_bytes = 0;
+    return ep_dispatch_ex(h, &args, stream, out);
+}
+
+ep_status ep_dispatch_ex(ep_handle *h, const ep_dispatch_args *args, void *stream, ep_dispatch_result *out)
+{
     if (!h)
         return fail(EP_ERR_INVALID_ARG, "handle is NULL");
+    if (!args)
+        return fail(EP_ERR_INVALID_ARG, "args is NULL");
     if (h->pending)
         return fail(EP_ERR_STATE, "dispatch called while the previous dispatch has not been combined");
+    const void *const *hidden = args->hidden;
+    const float *const *hidden_scale = args->hidden_scale;
+    const int32_t *const *topk_ids = args->topk_ids;
+    const float *const *topk_weights = args->topk_weights;
+    const int32_t *num_tokens = args->num_tokens;
+    const int runtime_max_tokens_per_rank = args->runtime_max_tokens_per_rank;
     if (!hidden || !topk_ids || !num_tokens)
         return fail(EP_ERR_INVALID_ARG, "hidden, topk_ids and num_tokens must not be NULL");
     ep_status st = check_device(h);
@@ -321,16 +407,31 @@ ep_status ep_dispatch(ep_handle *h, const void *const *hidden, const float *cons
         return fail(EP_ERR_INVALID_ARG, "runtime_max_tokens_per_rank=%d exceeds max_tokens_per_rank=%d",
                     T, h->capacity);
     uint64_t mask = 0;
-    st = resolve_mask(h, active_rank_mask, &mask);
+    st = resolve_mask(h, args->active_rank_mask, &mask);
     if (st != EP_OK)
         return st;
     if (hidden_scale && h->scale_cols == 0)
-        return fail(EP_ERR_INVALID_ARG, "hidden_scale needs hidden %% %d == 0 (hidden=%d)",
-                    EP_SCALE_GROUP, h->hidden);
+        return fail(EP_ERR_INVALID_ARG, "hidden_scale given but the handle has no scale columns "
+                                        "(hidden %% %d != 0 or scale_cols = 0)", EP_SCALE_GROUP);
+    const int eplb_bytes = args->eplb_local_stats ? args->eplb_stats_bytes : 0;
+    if (args->eplb_local_stats) {
+        if (h->eplb_max_bytes == 0)
+            return fail(EP_ERR_INVALID_ARG, "eplb_local_stats given but the handle was created without "
+                                            "eplb_stats_max_bytes");
+        if (eplb_bytes <= 0 || eplb_bytes % 4 != 0 || eplb_bytes > h->eplb_max_bytes)
+            return fail(EP_ERR_INVALID_ARG, "eplb_stats_bytes=%d must be a positive multiple of 4 "
+                                            "and at most %d", eplb_bytes, h->eplb_max_bytes);
+    }
 
     epk::DispatchArgs a;
     std::memset(&a, 0, sizeof a);
     for (int s = 0; s < h->ep; ++s) {
+        if (eplb_bytes) {
+            if (!args->eplb_local_stats[s] || !aligned(args->eplb_local_stats[s], 4))
+                return fail(EP_ERR_INVALID_ARG, "eplb_local_stats[%d] is NULL or not 4-byte aligned "
+                                                "(every rank passes its statistics)", s);
+            a.eplb_src[s] = static_cast<const uint8_t *>(args->eplb_local_stats[s]);
+        }
         const int n = num_tokens[s];
         if (n < 0 || n > T)
             return fail(EP_ERR_INVALID_ARG, "num_tokens[%d]=%d outside [0, tokens_per_rank=%d]", s, n, T);
@@ -370,6 +471,8 @@ ep_status ep_dispatch(ep_handle *h, const void *const *hidden, const float *cons
     a.row_bytes = h->row_bytes;
     a.G = hidden_scale ? h->scale_cols : 0;
     a.has_weights = topk_weights ? 1 : 0;
+    a.eplb_dst = h->ws + h->off_eplb;
+    a.eplb_bytes = eplb_bytes;
 
     cudaError_t ce = epk::launch_dispatch(a, static_cast<cudaStream_t>(stream));
     if (ce != cudaSuccess)
@@ -387,6 +490,8 @@ ep_status ep_dispatch(ep_handle *h, const void *const *hidden, const float *cons
         out->recv_scale = hidden_scale ? h->r_scale : nullptr;
         out->recv_topk_ids = h->r_ids;
         out->recv_topk_weights = topk_weights ? h->r_weights : nullptr;
+        out->eplb_global_stats = eplb_bytes ? h->ws + h->off_eplb : nullptr;
+        out->eplb_stats_bytes = eplb_bytes;
     }
     return ok();
 }

@@ -42,6 +42,11 @@ struct DispatchArgs {
     int row_bytes;  // hidden row bytes, a multiple of 16
     int G;          // scale columns per row (0 when no scales are sent)
     int has_weights;
+
+    // eplb_local_stats all-gather: rank r's eplb_bytes bytes -> eplb_dst + r*eplb_bytes
+    const uint8_t *eplb_src[kMaxEp];
+    uint8_t *eplb_dst;
+    int eplb_bytes;  // 0 = nothing to gather; else a multiple of 4
 };
 
 struct CombineArgs {

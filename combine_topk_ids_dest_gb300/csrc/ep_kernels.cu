@@ -122,6 +122,19 @@ __global__ void __launch_bounds__(kDispatchThreads)
     const long long warp_stride = (long long)gridDim.x * wpb;
     const int K = a.top_k;
 
+    // ---- eplb_local_stats all-gather: warp r copies rank r's statistics
+    // into row r of the gathered buffer (a few hundred bytes per rank).
+    if (a.eplb_bytes > 0) {
+        const long long gw = (long long)blockIdx.x * wpb + (threadIdx.x >> 5);
+        if (gw < a.ep) {
+            const int r = (int)gw;
+            const uint32_t *src = reinterpret_cast<const uint32_t *>(a.eplb_src[r]);
+            uint32_t *dst = reinterpret_cast<uint32_t *>(a.eplb_dst + (long long)r * a.eplb_bytes);
+            for (int w = lane; w < (a.eplb_bytes >> 2); w += 32)
+                dst[w] = src[w];
+        }
+    }
+
     for (long long slot = (long long)blockIdx.x * wpb + (threadIdx.x >> 5); slot < n_slots;
          slot += warp_stride) {
         const int s = (int)(slot / a.T);
@@ -343,13 +356,16 @@ int sm_count()
 cudaError_t launch_dispatch(const DispatchArgs &a, cudaStream_t stream)
 {
     const long long n_slots = (long long)a.ep * a.T;
-    if (n_slots == 0)
+    if (n_slots == 0 && a.eplb_bytes == 0)
         return cudaSuccess;
     const int wpb = kDispatchThreads / 32;
     long long blocks = (n_slots + wpb - 1) / wpb;
     const long long cap = (long long)sm_count() * kDispatchBlocksPerSm;
     if (blocks > cap)
         blocks = cap;
+    const long long eplb_blocks = a.eplb_bytes > 0 ? (a.ep + wpb - 1) / wpb : 0;  // one warp per rank
+    if (blocks < eplb_blocks)
+        blocks = eplb_blocks;
     dispatch_kernel<<<(unsigned)blocks, kDispatchThreads, 0, stream>>>(a);
     return cudaGetLastError();
 }

@@ -20,7 +20,8 @@ import torch
 from . import _lib
 from ._lib import ALL_RANKS, EpError, check, ptr_array
 
-_DTYPES = {torch.bfloat16: _lib.EP_DTYPE_BF16, torch.float8_e4m3fn: _lib.EP_DTYPE_FP8_E4M3}
+_DTYPES = {torch.bfloat16: _lib.EP_DTYPE_BF16, torch.float8_e4m3fn: _lib.EP_DTYPE_FP8_E4M3,
+           torch.float16: _lib.EP_DTYPE_FP16, torch.float32: _lib.EP_DTYPE_FP32}
 
 
 @dataclass
@@ -39,6 +40,9 @@ class EpDispatchResult:
     hidden_states_scale: Optional[List[torch.Tensor]]
     topk_ids: List[torch.Tensor]
     topk_weights: Optional[List[torch.Tensor]]
+    # every rank's eplb_local_stats stacked, [ep_size, *stats shape]; one
+    # tensor shared by all virtual ranks (treat as read-only), or None
+    eplb_global_stats: Optional[torch.Tensor] = None
 
 
 def _mask_value(m) -> int:
@@ -58,35 +62,42 @@ def _stream_ptr(device) -> int:
 class EpComm:
     """Rank-major MoE EP dispatch/combine over ``ep_size`` virtual ranks.
 
-    ``dtype`` is the hidden payload type: ``torch.bfloat16`` or
-    ``torch.float8_e4m3fn`` (fp8 rows usually travel with fp32 per-128-column
-    scales). The workspace is allocated here with torch, at capacity
-    ``max_tokens_per_rank``.
+    ``dtype`` is the hidden payload type: ``torch.bfloat16``,
+    ``torch.float8_e4m3fn`` (fp8 rows usually travel with fp32 scales),
+    ``torch.float16`` or ``torch.float32``. ``scale_cols`` is the number of
+    fp32 scales per row (default hidden/128 when that divides, else none).
+    ``eplb_stats_max_bytes`` reserves room to all-gather that many bytes of
+    ``eplb_local_stats`` per rank. The workspace is allocated here with
+    torch, at capacity ``max_tokens_per_rank``.
     """
 
     def __init__(self, ep_size: int, num_experts: int, top_k: int, hidden: int,
                  max_tokens_per_rank: int, dtype: torch.dtype = torch.bfloat16,
-                 enable_rank_mask: bool = False, device=None):
+                 enable_rank_mask: bool = False, device=None, scale_cols: Optional[int] = None,
+                 eplb_stats_max_bytes: int = 0):
         self._L = _lib.load()
         if dtype not in _DTYPES:
-            raise ValueError(f"dtype {dtype} not supported (bfloat16 or float8_e4m3fn)")
+            raise ValueError(f"dtype {dtype} not supported (bfloat16, float8_e4m3fn, float16, float32)")
         self.ep_size, self.num_experts, self.top_k = int(ep_size), int(num_experts), int(top_k)
         self.hidden, self.max_tokens_per_rank = int(hidden), int(max_tokens_per_rank)
         self.dtype, self.enable_rank_mask = dtype, bool(enable_rank_mask)
         self.device = torch.device("cuda", torch.cuda.current_device()) if device is None \
             else torch.device(device)
         self._h = None
+        if scale_cols is None:
+            scale_cols = self.hidden // _lib.EP_SCALE_GROUP if self.hidden % _lib.EP_SCALE_GROUP == 0 else 0
+        self.scale_cols = int(scale_cols)
+        self.eplb_stats_max_bytes = int(eplb_stats_max_bytes)
+        cfg = _lib.EpConfigC(self.ep_size, self.num_experts, self.top_k, self.hidden,
+                             self.max_tokens_per_rank, _DTYPES[dtype], int(self.enable_rank_mask),
+                             self.scale_cols, self.eplb_stats_max_bytes)
         nbytes = ctypes.c_size_t(0)
-        check(self._L.ep_workspace_size(self.ep_size, self.num_experts, self.top_k, self.hidden,
-                                        self.max_tokens_per_rank, _DTYPES[dtype],
-                                        ctypes.byref(nbytes)))
+        check(self._L.ep_workspace_size_ex(ctypes.byref(cfg), ctypes.byref(nbytes)))
         with torch.cuda.device(self.device):
             self._ws = torch.empty(nbytes.value, dtype=torch.uint8, device=self.device)
             h = ctypes.c_void_p()
-            check(self._L.ep_create_with_workspace(
-                self.ep_size, self.num_experts, self.top_k, self.hidden, self.max_tokens_per_rank,
-                _DTYPES[dtype], int(self.enable_rank_mask), ctypes.c_void_p(self._ws.data_ptr()),
-                nbytes.value, ctypes.byref(h)))
+            check(self._L.ep_create_ex(ctypes.byref(cfg), ctypes.c_void_p(self._ws.data_ptr()),
+                                       nbytes.value, ctypes.byref(h)))
         self._h = h
         self._counts: Optional[List[int]] = None
         self._T = 0
@@ -145,11 +156,11 @@ class EpComm:
         Per rank s: ``hidden_states[s]`` [n_s, hidden] (dtype of the
         communicator), ``topk_ids[s]`` int32 [n_s, top_k], optional
         ``topk_weights[s]`` fp32 [n_s, top_k] and ``hidden_states_scale[s]``
-        fp32 [n_s, hidden/128]. Weights and scales are all-or-none over ranks.
+        fp32 [n_s, scale_cols]. Weights and scales are all-or-none over ranks.
+        ``eplb_local_stats[s]`` (optional, every rank the same dtype and shape,
+        a multiple of 4 bytes) is gathered into ``eplb_global_stats``.
         """
         self._live()
-        if eplb_local_stats is not None:
-            raise NotImplementedError("eplb_local_stats is not supported by this backend")
         ep, K, H = self.ep_size, self.top_k, self.hidden
         if len(hidden_states) != ep or len(topk_ids) != ep:
             raise ValueError(f"hidden_states and topk_ids need {ep} per-rank tensors")
@@ -158,7 +169,20 @@ class EpComm:
                 raise ValueError(f"{name}: every rank passes it or none does "
                                  "(an empty rank passes an empty tensor)")
         counts = [int(x.shape[0]) for x in hidden_states]
-        G = H // _lib.EP_SCALE_GROUP
+        G = self.scale_cols
+        eplb_ptrs, eplb_bytes, eplb_meta = None, 0, None
+        if eplb_local_stats is not None:
+            if len(eplb_local_stats) != ep or any(x is None for x in eplb_local_stats):
+                raise ValueError("eplb_local_stats: every rank passes its statistics")
+            first = eplb_local_stats[0]
+            for s, x in enumerate(eplb_local_stats):
+                if x.dtype is not first.dtype or x.shape != first.shape or not x.is_contiguous() \
+                        or not x.is_cuda or x.get_device() != self._dev_index:
+                    raise ValueError(f"eplb_local_stats[{s}] must be a contiguous {first.dtype} "
+                                     f"{tuple(first.shape)} tensor on {self.device}")
+            eplb_bytes = first.numel() * first.element_size()
+            eplb_ptrs = ptr_array([x.data_ptr() for x in eplb_local_stats])
+            eplb_meta = (first.dtype, tuple(first.shape))
         for s in range(ep):
             n = counts[s]
             self._check_rank_tensor("hidden_states", hidden_states[s], s, n, H, self.dtype)
@@ -173,14 +197,17 @@ class EpComm:
         rt = -1 if runtime_max_tokens_per_rank is None else int(runtime_max_tokens_per_rank)
         if rt < -1:
             raise ValueError("runtime_max_tokens_per_rank must be >= 0")
-        with torch.cuda.device(self.device):
-            check(self._L.ep_dispatch(
-                self._h, ptr_array([x.data_ptr() for x in hidden_states]),
+        keep = (ptr_array([x.data_ptr() for x in hidden_states]),
                 ptr_array([x.data_ptr() for x in hidden_states_scale]) if hidden_states_scale is not None else None,
                 ptr_array([x.data_ptr() for x in topk_ids]),
-                ptr_array([x.data_ptr() for x in topk_weights]) if topk_weights is not None else None,
-                c_counts, rt, _mask_value(active_rank_mask), ctypes.c_void_p(_stream_ptr(self.device)),
-                ctypes.byref(res)))
+                ptr_array([x.data_ptr() for x in topk_weights]) if topk_weights is not None else None)
+        addr = lambda a: ctypes.cast(a, ctypes.c_void_p).value if a is not None else None
+        args = _lib.EpDispatchArgsC(addr(keep[0]), addr(keep[1]), addr(keep[2]), addr(keep[3]),
+                                    ctypes.cast(c_counts, ctypes.c_void_p).value, rt,
+                                    _mask_value(active_rank_mask), addr(eplb_ptrs), eplb_bytes)
+        with torch.cuda.device(self.device):
+            check(self._L.ep_dispatch_ex(self._h, ctypes.byref(args),
+                                         ctypes.c_void_p(_stream_ptr(self.device)), ctypes.byref(res)))
         T = res.tokens_per_rank
         self._counts, self._T = counts, T
         hs = self._rank_views("hidden", res.recv_hidden, T, H, self.dtype)
@@ -188,7 +215,11 @@ class EpComm:
         sc = self._rank_views("scale", res.recv_scale, T, G, torch.float32) if res.recv_scale else None
         w = self._rank_views("weights", res.recv_topk_weights, T, K, torch.float32) \
             if res.recv_topk_weights else None
-        return EpDispatchResult(T, hs, sc, ids, w)
+        stats = None
+        if eplb_meta is not None:
+            off = int(res.eplb_global_stats) - self._ws.data_ptr()
+            stats = self._ws[off:off + ep * eplb_bytes].view(eplb_meta[0]).view((ep,) + eplb_meta[1])
+        return EpDispatchResult(T, hs, sc, ids, w, stats)
 
     # -- MoEEpCommunication.get_combine_input_buffer ------------------------
     def get_combine_input_buffer(self, dtype: torch.dtype = torch.bfloat16, *, rank: Optional[int] = None):

@@ -60,14 +60,17 @@ typedef enum {
 } ep_status;
 
 typedef enum {
-    EP_DTYPE_BF16 = 0,     /* hidden rows of bfloat16 */
-    EP_DTYPE_FP8_E4M3 = 1  /* hidden rows of OCP fp8 e4m3fn */
+    EP_DTYPE_BF16 = 0,      /* hidden rows of bfloat16 */
+    EP_DTYPE_FP8_E4M3 = 1,  /* hidden rows of OCP fp8 e4m3fn */
+    EP_DTYPE_FP16 = 2,      /* hidden rows of IEEE binary16 */
+    EP_DTYPE_FP32 = 3       /* hidden rows of IEEE binary32 */
 } ep_dtype;
 
 #define EP_INVALID_EXPERT_ID (-1)
 #define EP_MAX_EP_SIZE 64 /* the rank mask is one uint64 */
 #define EP_MAX_TOP_K 32
-#define EP_SCALE_GROUP 128 /* hidden columns per fp32 scale */
+#define EP_SCALE_GROUP 128 /* hidden columns per fp32 scale (the default scale width) */
+#define EP_SCALE_COLS_DEFAULT (-1) /* ep_config.scale_cols: hidden/128 if that divides, else none */
 
 typedef struct ep_handle ep_handle;
 
@@ -80,10 +83,47 @@ typedef struct {
     int tokens_per_rank;
     int ep_size;
     void *const *recv_hidden;         /* rows of `hidden` elements of the payload dtype */
-    float *const *recv_scale;         /* rows of hidden/128 fp32, or NULL if none were sent */
+    float *const *recv_scale;         /* rows of scale_cols fp32, or NULL if none were sent */
     int32_t *const *recv_topk_ids;    /* rows of top_k int32 */
     float *const *recv_topk_weights;  /* rows of top_k fp32, or NULL if none were sent */
+    /* eplb_local_stats of all ranks, row r = rank r's bytes: device [ep_size,
+     * eplb_stats_bytes], one buffer every rank reads (treat as read-only), or
+     * NULL when the dispatch sent none (ep_dispatch_ex only). */
+    const void *eplb_global_stats;
+    int eplb_stats_bytes;
 } ep_dispatch_result;
+
+/* Everything a handle is created with (ep_create_ex). */
+typedef struct {
+    int ep_size;               /* 1..64 ranks */
+    int num_experts;           /* a positive multiple of ep_size */
+    int top_k;                 /* 1..32 */
+    int hidden;                /* payload columns; hidden*elem_bytes a multiple of 16, hidden % 8 == 0 */
+    int max_tokens_per_rank;   /* capacity C >= 0 */
+    ep_dtype dtype;            /* payload type of the hidden rows */
+    int enable_rank_mask;      /* 0/1 */
+    int scale_cols;            /* fp32 scales per row: EP_SCALE_COLS_DEFAULT, 0 (none) or > 0 */
+    int eplb_stats_max_bytes;  /* eplb_local_stats bytes per rank the handle can gather, a
+                                  multiple of 4 (0: not supported) */
+} ep_config;
+
+/* Everything one dispatch takes (ep_dispatch_ex); see ep_dispatch for the
+ * first seven fields. eplb_local_stats: NULL, or eplb_local_stats[r] =
+ * device pointer to rank r's eplb_stats_bytes bytes of expert-load
+ * statistics (4-byte aligned; every rank passes the same size), gathered
+ * into ep_dispatch_result.eplb_global_stats by the same launch
+ * (MoEEpCommunication.dispatch, parameter eplb_local_stats). */
+typedef struct {
+    const void *const *hidden;
+    const float *const *hidden_scale;
+    const int32_t *const *topk_ids;
+    const float *const *topk_weights;
+    const int32_t *num_tokens;
+    int runtime_max_tokens_per_rank;
+    uint64_t active_rank_mask;
+    const void *const *eplb_local_stats;
+    int eplb_stats_bytes;
+} ep_dispatch_args;
 
 /* 1 when the current CUDA device can run this library (compute capability
  * 10.3, the sm_103a build), else 0. Does no GPU work.
@@ -96,6 +136,9 @@ int ep_is_supported(void);
  * Validates the parameters like ep_create. */
 ep_status ep_workspace_size(int ep_size, int num_experts, int top_k, int hidden,
                             int max_tokens_per_rank, ep_dtype dtype, size_t *bytes);
+
+/* ep_workspace_size for a full configuration (scale width, eplb capacity). */
+ep_status ep_workspace_size_ex(const ep_config *cfg, size_t *bytes);
 
 /* Creates a handle for one EP group (MoEEpCommunication constructor with
  * MoEEpCommParams). Requirements: 1 <= ep_size <= 64; num_experts a
@@ -115,11 +158,18 @@ ep_status ep_create_with_workspace(int ep_size, int num_experts, int top_k, int 
                                    int max_tokens_per_rank, ep_dtype dtype, int enable_rank_mask,
                                    void *workspace, size_t bytes, ep_handle **out);
 
+/* Creates a handle from a full configuration. workspace == NULL: allocate
+ * with cudaMalloc (freed by ep_destroy); else caller-owned device memory of
+ * `bytes` >= ep_workspace_size_ex, 256-byte aligned. ep_create(...) equals
+ * ep_create_ex with scale_cols = EP_SCALE_COLS_DEFAULT and
+ * eplb_stats_max_bytes = 0. */
+ep_status ep_create_ex(const ep_config *cfg, void *workspace, size_t bytes, ep_handle **out);
+
 /* Dispatch of all ep_size source ranks (MoEEpCommunication.dispatch;
  * NVLinkOneSidedAlltoAll.dispatch for active_rank_mask).
  *  hidden[s]       device [num_tokens[s], hidden] payload dtype, 16-byte aligned
- *  hidden_scale    NULL, or hidden_scale[s] device fp32 [num_tokens[s], hidden/128]
- *                  (needs hidden % 128 == 0)
+ *  hidden_scale    NULL, or hidden_scale[s] device fp32 [num_tokens[s], scale_cols]
+ *                  (scale_cols = hidden/128 for ep_create handles; needs scale_cols > 0)
  *  topk_ids[s]     device int32 [num_tokens[s], top_k], global expert ids
  *  topk_weights    NULL, or topk_weights[s] device fp32 [num_tokens[s], top_k]
  *  num_tokens      host int32 [ep_size], 0 <= num_tokens[s] <= tokens_per_rank
@@ -138,6 +188,13 @@ ep_status ep_dispatch(ep_handle *h, const void *const *hidden, const float *cons
                       const int32_t *const *topk_ids, const float *const *topk_weights,
                       const int32_t *num_tokens, int runtime_max_tokens_per_rank,
                       uint64_t active_rank_mask, void *stream, ep_dispatch_result *out);
+
+/* ep_dispatch with its arguments in a struct, plus the eplb_local_stats
+ * all-gather. Same checks and errors; additionally EP_ERR_INVALID_ARG when
+ * stats are given to a handle without eplb capacity, exceed it, are not a
+ * multiple of 4 bytes, or are missing for some rank. */
+ep_status ep_dispatch_ex(ep_handle *h, const ep_dispatch_args *args, void *stream,
+                         ep_dispatch_result *out);
 
 /* Device pointer to rank `rank`'s backend-owned combine input: bf16
  * [ep_size*tokens_per_rank, hidden] of the pending dispatch. Passing it (or

@@ -72,6 +72,8 @@ def lib() -> ctypes.CDLL:
             L.oracle_identity_expert.argtypes = [i32, i32, i32, i32, i32, i32, i32,
                                                  P, P, P, P, P]
             L.oracle_identity_expert.restype = i32
+            L.oracle_eplb_gather.argtypes = [i32, i32, P, P]
+            L.oracle_eplb_gather.restype = i32
             _lib = L
     return _lib
 
@@ -248,3 +250,14 @@ def identity_expert(ep_size: int, num_experts: int, top_k: int, hidden: int, ele
     if rc != 0:
         raise ValueError("oracle_identity_expert: inconsistent sizes")
     return eo
+
+
+def eplb_gather(local: Sequence) -> np.ndarray:
+    """uint8 [ep, bytes]: row r = rank r's statistics bytes (see ep_oracle.c)."""
+    arrs = [np.ascontiguousarray(_np(x)).view(np.uint8).reshape(-1) for x in local]
+    nbytes = arrs[0].size
+    out = np.zeros((len(arrs), nbytes), np.uint8)
+    p_loc, k = _ptrs(arrs)
+    if lib().oracle_eplb_gather(len(arrs), nbytes, _voidp(p_loc), out.ctypes.data) != 0:
+        raise ValueError("oracle_eplb_gather: inconsistent sizes")
+    return out

@@ -216,6 +216,21 @@ int oracle_combine(int ep_size, int num_experts, int top_k, int hidden, int toke
     return 0;
 }
 
+/* ---- eplb statistics all-gather ----------------------------------------- */
+
+/* Every rank's expert-load statistics gathered alongside the dispatch
+ * ("flashinfer.moe_ep.MoEEpCommunication", dispatch(), parameter
+ * eplb_local_stats): row r of `global` is rank r's `bytes` bytes. */
+int oracle_eplb_gather(int ep_size, int bytes, const uint8_t *const *local, uint8_t *global)
+{
+    if (ep_size < 1 || ep_size > ORACLE_MAX_EP || bytes < 0)
+        return -1;
+    for (int r = 0; r < ep_size; ++r)
+        for (int b = 0; b < bytes; ++b)
+            global[(long)r * bytes + b] = local[r][b];
+    return 0;
+}
+
 /* ---- identity expert (outside the method; used by invariant tests) ------ */
 
 /* What a rank whose experts are all the identity would hand to combine:

@@ -74,11 +74,11 @@ def gpu_round(inp, device, special=False, caller_eo=False, comm=None, keep=False
     Returns host copies of the receive buffers and outputs."""
     from combine_topk_ids_dest_gb300 import EpComm
     wl = inp.wl
-    dtype = torch.bfloat16 if wl.dtype == "bf16" else torch.float8_e4m3fn
     own = comm is None
     if own:
-        comm = EpComm(wl.ep_size, wl.num_experts, wl.top_k, wl.hidden, wl.capacity, dtype=dtype,
-                      enable_rank_mask=wl.enable_rank_mask, device=device)
+        comm = EpComm(wl.ep_size, wl.num_experts, wl.top_k, wl.hidden, wl.capacity, dtype=wl.torch_dtype,
+                      enable_rank_mask=wl.enable_rank_mask, device=device,
+                      scale_cols=wl.scale_cols if wl.scales else None)
     mask = inp.active_rank_mask if wl.enable_rank_mask else None
     res = comm.dispatch(to_dev(inp.hidden, device), to_dev(inp.topk_ids, device),
                         to_dev(inp.topk_weights, device),

@@ -45,7 +45,7 @@ def test_full_size_sampled(cuda_device, name):
     wl = workloads.WORKLOADS[name]
     inp = workloads.make_inputs(wl)
     ep, E, K, H = wl.ep_size, wl.num_experts, wl.top_k, wl.hidden
-    dtype = torch.bfloat16 if wl.dtype == "bf16" else torch.float8_e4m3fn
+    dtype = wl.torch_dtype
     comm = EpComm(ep, E, K, H, wl.capacity, dtype=dtype, enable_rank_mask=wl.enable_rank_mask,
                   device=cuda_device)
     try:

@@ -71,6 +71,10 @@ BASE = workloads.EpWorkload(name="edge", ep_size=4, num_experts=16, top_k=4, hid
     dict(dtype="fp8_e4m3", hidden=256, scales=True),
     dict(dtype="fp8_e4m3", hidden=272, scales=False),      # fp8 row not a multiple of 128
     dict(dtype="bf16", hidden=384, scales=True),           # scales with a bf16 payload
+    dict(dtype="fp16", scales=True),                       # fp16 payload, hidden/128 scales
+    dict(dtype="fp32", hidden=264),                        # fp32 payload (1056-byte rows)
+    dict(dtype="bf16", scales=True, scale_cols_override=7),  # odd scale width
+    dict(dtype="fp8_e4m3", hidden=512, scales=True, scale_cols_override=16),  # 32-column groups
     dict(hidden=8),                                        # one 16-byte vector per row
     dict(hidden=264),                                      # combine: 33 vectors, ragged block
 ])

@@ -37,7 +37,7 @@ class EpWorkload:
     num_experts: int
     top_k: int
     hidden: int
-    dtype: str  # "bf16" or "fp8_e4m3"
+    dtype: str  # "bf16", "fp8_e4m3", "fp16" or "fp32"
     capacity: int  # max_tokens_per_rank
     runtime_max: Optional[int]  # runtime_max_tokens_per_rank (None = capacity)
     counts: tuple = ("fixed",)  # ("fixed", c0, c1, ...), ("uniform", lo, hi), ("full",)
@@ -48,6 +48,7 @@ class EpWorkload:
     scales: bool = False
     dropped_ranks: Optional[tuple] = None  # ranks left out of active_rank_mask
     seed: int = 0
+    scale_cols_override: Optional[int] = None  # scale columns when not hidden/128
 
     @property
     def tokens_per_rank(self) -> int:
@@ -59,11 +60,20 @@ class EpWorkload:
 
     @property
     def elem_bytes(self) -> int:
-        return 2 if self.dtype == "bf16" else 1
+        return {"bf16": 2, "fp16": 2, "fp8_e4m3": 1, "fp32": 4}[self.dtype]
+
+    @property
+    def torch_dtype(self):
+        return {"bf16": torch.bfloat16, "fp16": torch.float16, "fp8_e4m3": torch.float8_e4m3fn,
+                "fp32": torch.float32}[self.dtype]
 
     @property
     def scale_cols(self) -> int:
-        return self.hidden // SCALE_GROUP if self.scales else 0
+        if not self.scales:
+            return 0
+        if self.scale_cols_override is not None:
+            return self.scale_cols_override
+        return self.hidden // SCALE_GROUP
 
     def active_ranks(self) -> list:
         drop = set(self.dropped_ranks or ())
@@ -193,10 +203,13 @@ def make_inputs(wl: EpWorkload) -> EpInputs:
     hidden, scale = [], ([] if wl.scales else None)
     for n in counts:
         x = torch.randn(n, wl.hidden, generator=g)
-        if wl.dtype == "bf16":
-            hidden.append(x.to(torch.bfloat16).contiguous())
+        if wl.dtype in ("bf16", "fp16", "fp32"):
+            hidden.append(x.to(wl.torch_dtype).contiguous())
             if wl.scales:
                 scale.append(torch.rand(n, wl.scale_cols, generator=g).to(torch.float32) + 0.5)
+        elif wl.scales and wl.scale_cols_override is not None:  # fp8 rows with a custom scale width
+            hidden.append(x.clamp(-FP8_MAX, FP8_MAX).to(torch.float8_e4m3fn).contiguous())
+            scale.append(torch.rand(n, wl.scale_cols, generator=g).to(torch.float32) + 0.5)
         elif wl.scales:
             q, s = quantize_fp8_groups(x)
             hidden.append(q)
