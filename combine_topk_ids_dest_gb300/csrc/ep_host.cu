@@ -539,8 +539,10 @@ ep_status ep_combine(ep_handle *h, const void *const *expert_output, void *const
             return fail(EP_ERR_INVALID_ARG, "expert_output[%d] is not 16-byte aligned", d);
         a.eo[d] = static_cast<const uint16_t *>(p);
     }
+    a.token_offset[0] = 0;
     for (int s = 0; s < h->ep; ++s) {
         a.num_tokens[s] = h->counts[s];
+        a.token_offset[s + 1] = a.token_offset[s] + h->counts[s];
         if (h->counts[s] == 0)
             continue;
         if (!output[s] || !aligned(output[s], 16))

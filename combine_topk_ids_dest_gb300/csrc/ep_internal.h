@@ -53,7 +53,9 @@ struct CombineArgs {
     const uint16_t *eo[kMaxEp];  // rank d's bf16 combine input, [ep*T, H]
     uint16_t *out[kMaxEp];       // source rank s's bf16 output, [num_tokens[s], H]
     int num_tokens[kMaxEp];
-    const uint64_t *route_mask;  // [ep*T], written by the dispatch
+    int token_offset[kMaxEp + 1];  // prefix sums of num_tokens: live token g of rank s has
+                                   // token_offset[s] <= g < token_offset[s+1]
+    const uint64_t *route_mask;    // [ep*T], written by the dispatch
     int ep, T, H;
 };
 

@@ -141,6 +141,20 @@ __global__ void __launch_bounds__(kDispatchThreads)
         const int t = (int)(slot - (long long)s * a.T);
         const bool live = t < a.num_tokens[s];
 
+        // ---- first chunk of the hidden row, issued before the routing so the
+        // two memory round trips overlap (almost every live token is routed)
+        const int nvec = a.row_bytes >> 4;
+        const uint8_t *src = a.hidden[s] + (long long)t * a.row_bytes;
+        uint4 v[kDispatchVecPerLane];
+        if (live) {
+#pragma unroll
+            for (int j = 0; j < kDispatchVecPerLane; ++j) {
+                const int idx = j * 32 + lane;
+                if (idx < nvec)
+                    v[j] = ld_stream(src + 16 * (long long)idx);
+            }
+        }
+
         // ---- routing: destination-rank bit set of this slot
         int my_id = EP_INVALID_EXPERT_ID;
         unsigned lo = 0, hi = 0;
@@ -199,16 +213,15 @@ __global__ void __launch_bounds__(kDispatchThreads)
             continue;  // warp-uniform: padding, unrouted or fully masked slot
 
         // ---- hidden row: read once, store to each routed rank
-        const int nvec = a.row_bytes >> 4;
-        const uint8_t *src = a.hidden[s] + (long long)t * a.row_bytes;
         uint8_t *dst_slot = a.recv_hidden + slot * a.row_bytes;
         for (int c0 = 0; c0 < nvec; c0 += 32 * kDispatchVecPerLane) {
-            uint4 v[kDispatchVecPerLane];
+            if (c0 > 0) {
 #pragma unroll
-            for (int j = 0; j < kDispatchVecPerLane; ++j) {
-                const int idx = c0 + j * 32 + lane;
-                if (idx < nvec)
-                    v[j] = ld_stream(src + 16 * (long long)idx);
+                for (int j = 0; j < kDispatchVecPerLane; ++j) {
+                    const int idx = c0 + j * 32 + lane;
+                    if (idx < nvec)
+                        v[j] = ld_stream(src + 16 * (long long)idx);
+                }
             }
             for (uint64_t mm = m; mm; mm &= mm - 1) {
                 const int d = __ffsll((long long)mm) - 1;
@@ -251,12 +264,21 @@ __global__ void __launch_bounds__(kCombineMaxThreads)
     const int nvec = a.H >> 3;  // 8 bf16 per 16-byte vector
     const int nthr = blockDim.x;
     for (long long b = blockIdx.x; b < n_blocks; b += gridDim.x) {
-        const long long slot = b / blocks_per_row;
-        const int chunk = (int)(b - slot * blocks_per_row);
-        const int s = (int)(slot / a.T);
-        const int t = (int)(slot - (long long)s * a.T);
-        if (t >= a.num_tokens[s])
-            continue;  // block-uniform
+        // block -> (live token g, column chunk); g -> source rank s by binary
+        // search of the token offsets, so no block is spent on padding slots
+        const int g = (int)(b / blocks_per_row);
+        const int chunk = (int)(b - (long long)g * blocks_per_row);
+        int lo = 0, hi = a.ep - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (a.token_offset[mid] <= g)
+                lo = mid;
+            else
+                hi = mid - 1;
+        }
+        const int s = lo;
+        const int t = g - a.token_offset[s];
+        const long long slot = (long long)s * a.T + t;
         const int v0 = chunk * (nthr * kCombineVpt) + threadIdx.x;
         if (v0 >= nvec)
             continue;
@@ -376,7 +398,7 @@ cudaError_t launch_combine(const CombineArgs &a, cudaStream_t stream)
     const int threads = combine_threads(nvec);
     const int per_block = threads * kCombineVpt;
     const int bpr = (nvec + per_block - 1) / per_block;
-    const long long n_blocks = (long long)a.ep * a.T * bpr;
+    const long long n_blocks = (long long)a.token_offset[a.ep] * bpr;
     if (n_blocks == 0)
         return cudaSuccess;
     long long grid = n_blocks;
