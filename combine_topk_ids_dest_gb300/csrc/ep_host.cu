@@ -31,6 +31,8 @@
 #include <cstring>
 #include <new>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "ep_internal.h"
 
 struct ep_handle {
@@ -474,7 +476,9 @@ ep_status ep_dispatch_ex(ep_handle *h, const ep_dispatch_args *args, void *strea
     a.eplb_dst = h->ws + h->off_eplb;
     a.eplb_bytes = eplb_bytes;
 
+    nvtxRangePushA("ep_dispatch");  // host-side range around the launch, for profilers
     cudaError_t ce = epk::launch_dispatch(a, static_cast<cudaStream_t>(stream));
+    nvtxRangePop();
     if (ce != cudaSuccess)
         return fail(EP_ERR_CUDA, "dispatch launch: %s", cudaGetErrorString(ce));
 
@@ -554,7 +558,9 @@ ep_status ep_combine(ep_handle *h, const void *const *expert_output, void *const
     a.T = h->T;
     a.H = h->hidden;
 
+    nvtxRangePushA("ep_combine");
     cudaError_t ce = epk::launch_combine(a, static_cast<cudaStream_t>(stream));
+    nvtxRangePop();
     if (ce != cudaSuccess)
         return fail(EP_ERR_CUDA, "combine launch: %s", cudaGetErrorString(ce));
     h->pending = false;

@@ -35,7 +35,7 @@ namespace {
 #define EP_DISPATCH_THREADS 256
 #endif
 #ifndef EP_DISPATCH_VEC_PER_LANE
-#define EP_DISPATCH_VEC_PER_LANE 16
+#define EP_DISPATCH_VEC_PER_LANE 8
 #endif
 #ifndef EP_DISPATCH_BLOCKS_PER_SM
 #define EP_DISPATCH_BLOCKS_PER_SM 64
@@ -135,21 +135,32 @@ __global__ void __launch_bounds__(kDispatchThreads)
         }
     }
 
-    for (long long slot = (long long)blockIdx.x * wpb + (threadIdx.x >> 5); slot < n_slots;
-         slot += warp_stride) {
+    // Work items are (slot, column chunk) pairs: the hidden row is split into
+    // chunks of 32*kDispatchVecPerLane 16-byte vectors, one warp per chunk,
+    // so the work divides finely over the resident warps even when there are
+    // few slots. Every item routes its slot; the first chunk's item also
+    // writes the routing state, the id plane and the scale/weight rows.
+    const int nvec = a.row_bytes >> 4;
+    const int chunk_vecs = 32 * kDispatchVecPerLane;
+    const int nchunks = (nvec + chunk_vecs - 1) / chunk_vecs;
+    const long long n_items = n_slots * nchunks;
+    for (long long item = (long long)blockIdx.x * wpb + (threadIdx.x >> 5); item < n_items;
+         item += warp_stride) {
+        const long long slot = item / nchunks;
+        const int chunk = (int)(item - slot * nchunks);
+        const int c0 = chunk * chunk_vecs;
         const int s = (int)(slot / a.T);
         const int t = (int)(slot - (long long)s * a.T);
         const bool live = t < a.num_tokens[s];
 
-        // ---- first chunk of the hidden row, issued before the routing so the
+        // ---- this chunk of the hidden row, loaded before the routing so the
         // two memory round trips overlap (almost every live token is routed)
-        const int nvec = a.row_bytes >> 4;
         const uint8_t *src = a.hidden[s] + (long long)t * a.row_bytes;
         uint4 v[kDispatchVecPerLane];
         if (live) {
 #pragma unroll
             for (int j = 0; j < kDispatchVecPerLane; ++j) {
-                const int idx = j * 32 + lane;
+                const int idx = c0 + j * 32 + lane;
                 if (idx < nvec)
                     v[j] = ld_stream(src + 16 * (long long)idx);
             }
@@ -171,12 +182,14 @@ __global__ void __launch_bounds__(kDispatchThreads)
         lo = __reduce_or_sync(kFull, lo);
         hi = __reduce_or_sync(kFull, hi);
         const uint64_t m = ((((uint64_t)hi) << 32) | lo) & a.active;
-        if (lane == 0)
+        if (chunk == 0 && lane == 0)
             a.route_mask[slot] = m;
 
-        // ---- id rows of this slot in all destination ranks
+        // ---- id rows of this slot in all destination ranks (first chunk's item)
         int32_t *ids_slot = a.recv_ids + slot * K;
-        if ((K & 3) == 0) {
+        if (chunk != 0) {
+            // the first chunk's item writes the slot's ids
+        } else if ((K & 3) == 0) {
             const int qpr = K >> 2;  // int4 vectors per id row
             const int n = a.ep * qpr;
             for (int base = 0; base < n; base += 32) {
@@ -212,28 +225,20 @@ __global__ void __launch_bounds__(kDispatchThreads)
         if (m == 0)
             continue;  // warp-uniform: padding, unrouted or fully masked slot
 
-        // ---- hidden row: read once, store to each routed rank
+        // ---- this chunk of the hidden row: read once, stored to each routed rank
         uint8_t *dst_slot = a.recv_hidden + slot * a.row_bytes;
-        for (int c0 = 0; c0 < nvec; c0 += 32 * kDispatchVecPerLane) {
-            if (c0 > 0) {
+        for (uint64_t mm = m; mm; mm &= mm - 1) {
+            const int d = __ffsll((long long)mm) - 1;
+            uint4 *dst = reinterpret_cast<uint4 *>(dst_slot + d * a.hidden_stride);
 #pragma unroll
-                for (int j = 0; j < kDispatchVecPerLane; ++j) {
-                    const int idx = c0 + j * 32 + lane;
-                    if (idx < nvec)
-                        v[j] = ld_stream(src + 16 * (long long)idx);
-                }
-            }
-            for (uint64_t mm = m; mm; mm &= mm - 1) {
-                const int d = __ffsll((long long)mm) - 1;
-                uint4 *dst = reinterpret_cast<uint4 *>(dst_slot + d * a.hidden_stride);
-#pragma unroll
-                for (int j = 0; j < kDispatchVecPerLane; ++j) {
-                    const int idx = c0 + j * 32 + lane;
-                    if (idx < nvec)
-                        st_row(dst + idx, v[j]);
-                }
+            for (int j = 0; j < kDispatchVecPerLane; ++j) {
+                const int idx = c0 + j * 32 + lane;
+                if (idx < nvec)
+                    st_row(dst + idx, v[j]);
             }
         }
+        if (chunk != 0)
+            continue;
 
         // ---- scale row (G fp32) and weight row (K fp32)
         if (a.G > 0) {
@@ -381,7 +386,9 @@ cudaError_t launch_dispatch(const DispatchArgs &a, cudaStream_t stream)
     if (n_slots == 0 && a.eplb_bytes == 0)
         return cudaSuccess;
     const int wpb = kDispatchThreads / 32;
-    long long blocks = (n_slots + wpb - 1) / wpb;
+    const int chunk_vecs = 32 * kDispatchVecPerLane;
+    const long long n_items = n_slots * (((a.row_bytes >> 4) + chunk_vecs - 1) / chunk_vecs);
+    long long blocks = (n_items + wpb - 1) / wpb;
     const long long cap = (long long)sm_count() * kDispatchBlocksPerSm;
     if (blocks > cap)
         blocks = cap;

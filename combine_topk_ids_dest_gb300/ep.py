@@ -300,6 +300,9 @@ class EpComm:
     def __del__(self):
         try:
             if getattr(self, "_h", None) is not None:
+                # work queued on any stream may still use the workspace, which
+                # torch frees (and may hand out again) once this object is gone
+                torch.cuda.synchronize(self.device)
                 self._L.ep_destroy(self._h)
                 self._h = None
         except Exception:

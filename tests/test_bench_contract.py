@@ -1,0 +1,73 @@
+"""CPU checks of bench.py's host logic: the reference arm's JSON line, the
+argument rules, the non-zero ranks' silence under torchrun, and the
+algorithmic byte count (its routed-pair count P against the oracle's
+receive planes)."""
+import json
+import os
+import subprocess
+import sys
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _bench(*args, env=None):
+    e = dict(os.environ)
+    e.update(env or {})
+    return subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), *args], capture_output=True,
+                          text=True, env=e, timeout=300)
+
+
+def test_reference_arm_line():
+    r = _bench("--impl", "reference", "--workload", "tiny", "--steps", "3", "--warmup", "3",
+               "--reference-seconds", "3")
+    assert r.returncode == 0, r.stderr
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e", "impl"):
+        assert key in line, key
+    assert line["impl"] == "reference" and line["unit"] == "GB/s" and line["higher_is_better"] is True
+    assert line["steps"] == 3 and line["warmup"] == 3 and line["value"] > 0
+    assert line["config"]["workload"] == "tiny"
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] == 1 and cb["value"] == line["value"]
+    assert line["e2e"] == {"value": line["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
+
+
+def test_reference_arm_nonzero_rank_is_silent():
+    r = _bench("--impl", "reference", "--workload", "tiny", "--steps", "3", "--warmup", "3",
+               env={"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"})
+    assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def test_warmup_below_three_is_rejected():
+    r = _bench("--impl", "reference", "--workload", "tiny", "--steps", "3", "--warmup", "2")
+    assert r.returncode != 0
+
+
+@pytest.mark.parametrize("name", ["tiny", "qwen3_mask"])
+def test_round_bytes_routed_pairs_match_oracle(name):
+    import bench
+    from ep_testutil import small
+    wl = workloads.WORKLOADS[name]
+    wl = wl if name == "tiny" else small(wl)
+    inp = workloads.make_inputs(wl)
+    b = bench.round_bytes(inp)
+    disp = oracle.dispatch(wl.ep_size, wl.num_experts, wl.top_k, wl.tokens_per_rank, inp.num_tokens,
+                           inp.hidden, inp.topk_ids, mask_enabled=wl.enable_rank_mask,
+                           active_rank_mask=inp.active_rank_mask, payload=False)
+    P = sum(int((ids != -1).any(axis=1).sum()) for ids in disp.recv_ids)
+    assert b["P"] == P and b["N"] == inp.total_tokens
+    ep, K, H, T = wl.ep_size, wl.top_k, wl.hidden, wl.tokens_per_rank
+    hb = H * wl.elem_bytes
+    G = wl.scale_cols
+    w = 1 if inp.topk_weights is not None else 0
+    N = inp.total_tokens
+    assert b["total"] == (N * (hb + 4 * G + 4 * K + 4 * K * w) + P * (hb + 4 * G + 4 * K * w)
+                          + ep * ep * T * 4 * K + P * 2 * H + 8 * N + N * 2 * H)

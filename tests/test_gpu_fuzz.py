@@ -1,0 +1,52 @@
+"""Randomised GPU parity: many small seeded geometries (ep_size, experts per
+rank, top_k, hidden width, payload dtype, scale width, counts, tokens per rank,
+masks, id laws, weights on/off, caller-owned or backend expert outputs), each
+compared bit for bit with the oracle."""
+import random
+
+import pytest
+
+import workloads
+from ep_testutil import assert_round_equal, gpu_round, oracle_round
+
+pytestmark = pytest.mark.gpu
+
+N_CASES = 40
+
+
+def _case(seed):
+    rng = random.Random(1000 + seed)
+    ep = rng.choice([1, 2, 3, 4, 5, 8, 13, 16, 31, 33, 64])
+    epr = rng.choice([1, 2, 3, 4, 8])
+    E = ep * epr
+    K = rng.randint(1, min(E, 12)) if rng.random() < 0.8 else rng.randint(1, 32)
+    dtype = rng.choice(["bf16", "fp8_e4m3", "fp16", "fp32"])
+    align = {"bf16": 8, "fp16": 8, "fp8_e4m3": 16, "fp32": 8}[dtype]
+    hidden = align * rng.randint(1, 96)
+    scales = rng.random() < 0.5
+    scale_cols = None
+    if scales and (hidden % 128 != 0 or rng.random() < 0.5):
+        scale_cols = rng.randint(1, 20)
+    cap = rng.randint(0, 12)
+    rt = None if rng.random() < 0.5 else rng.randint(0, cap)
+    T = cap if rt is None else rt
+    counts = ("uniform", 0, T) if rng.random() < 0.7 else ("full",)
+    ids = "uniform_distinct" if K <= E else "uniform_dups"
+    ids = rng.choice([ids, "uniform_dups", "with_invalid"]) if K <= E else ids
+    dropped = None
+    if rng.random() < 0.4:
+        dropped = tuple(r for r in range(ep) if rng.random() < 0.3)
+    return workloads.EpWorkload(
+        name=f"fuzz{seed}", ep_size=ep, num_experts=E, top_k=K, hidden=hidden, dtype=dtype,
+        capacity=cap, runtime_max=rt, counts=counts, ids=ids, weights=rng.random() < 0.7,
+        scales=scales, scale_cols_override=scale_cols, dropped_ranks=dropped, seed=seed), \
+        rng.random() < 0.3
+
+
+@pytest.mark.parametrize("seed", range(N_CASES))
+def test_random_geometry(cuda_device, seed):
+    wl, caller_eo = _case(seed)
+    inp = workloads.make_inputs(wl)
+    got = gpu_round(inp, cuda_device, caller_eo=caller_eo)
+    disp, out = oracle_round(inp)
+    assert_round_equal(inp, got, disp, out)
