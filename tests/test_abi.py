@@ -103,3 +103,54 @@ def test_create_without_gpu_reports_error():
     assert h.value is None
     assert L.ep_is_supported() == 0
     assert not ep.EpComm.is_platform_supported()
+
+
+def _size_ex(**kw):
+    base = dict(ep_size=4, num_experts=8, top_k=2, hidden=256, max_tokens_per_rank=16, dtype=0,
+                enable_rank_mask=0, scale_cols=-1, eplb_stats_max_bytes=0)
+    base.update(kw)
+    cfg = _lib.EpConfigC(*[base[f] for f, _ in _lib.EpConfigC._fields_])
+    n = ctypes.c_size_t(0)
+    st = _lib.load().ep_workspace_size_ex(ctypes.byref(cfg), ctypes.byref(n))
+    return st, n.value
+
+
+@pytest.mark.parametrize("dtype,elem", [(0, 2), (1, 1), (2, 2), (3, 4)])
+@pytest.mark.parametrize("scale_cols,G", [(-1, 2), (0, 0), (7, 7)])
+@pytest.mark.parametrize("eplb", [0, 1024])
+def test_workspace_size_ex_formula(dtype, elem, scale_cols, G, eplb):
+    st, n = _size_ex(dtype=dtype, scale_cols=scale_cols, eplb_stats_max_bytes=eplb)
+    assert st == ep.EP_OK
+    ep_size, K, H, C = 4, 2, 256, 16
+    rows = ep_size * C
+    want = ep_size * (_align(rows * H * elem) + _align(rows * G * 4) + _align(rows * K * 4) * 2 +
+                      _align(rows * H * 2)) + _align(rows * 8) + _align(ep_size * eplb)
+    assert n == want
+
+
+def test_default_config_matches_plain_workspace_size():
+    assert _size_ex() == _size(4, 8, 2, 256, 16, 0)
+
+
+@pytest.mark.parametrize("kw,frag", [
+    (dict(scale_cols=-2), "scale_cols"),
+    (dict(eplb_stats_max_bytes=6), "eplb_stats_max_bytes"),
+    (dict(eplb_stats_max_bytes=-4), "eplb_stats_max_bytes"),
+    (dict(dtype=4), "dtype"),
+    (dict(dtype=3, hidden=12), "hidden % 8"),   # 48-byte fp32 rows, but combine needs 8 | hidden
+    (dict(dtype=1, hidden=24), "16 bytes"),     # 24-byte fp8 rows
+])
+def test_workspace_size_ex_rejects(kw, frag):
+    st, _ = _size_ex(**kw)
+    assert st == ep.EP_ERR_INVALID_ARG
+    assert frag in _lib.load().ep_last_error().decode()
+
+
+def test_null_config_and_args_rejected():
+    L = _lib.load()
+    n = ctypes.c_size_t(0)
+    assert L.ep_workspace_size_ex(None, ctypes.byref(n)) == ep.EP_ERR_INVALID_ARG
+    h = ctypes.c_void_p()
+    assert L.ep_create_ex(None, None, 0, ctypes.byref(h)) == ep.EP_ERR_INVALID_ARG
+    res = _lib.EpDispatchResultC()
+    assert L.ep_dispatch_ex(None, None, None, ctypes.byref(res)) == ep.EP_ERR_INVALID_ARG
