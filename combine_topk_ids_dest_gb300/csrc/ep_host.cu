@@ -143,6 +143,9 @@ ep_status plan(const ep_config *cfg, Layout *L)
         return fail(EP_ERR_INVALID_ARG, "hidden=%d: the bf16 combine rows need hidden %% 8 == 0", H);
     if (C < 0)
         return fail(EP_ERR_INVALID_ARG, "max_tokens_per_rank=%d < 0", C);
+    if ((long long)ep * C > (1LL << 30))  // slot and token indices are 32-bit in the kernels
+        return fail(EP_ERR_INVALID_ARG, "ep_size*max_tokens_per_rank=%lld exceeds 2^30 slots",
+                    (long long)ep * C);
     if (cfg->scale_cols < EP_SCALE_COLS_DEFAULT)
         return fail(EP_ERR_INVALID_ARG, "scale_cols=%d: use -1 (default), 0 or a positive count",
                     cfg->scale_cols);

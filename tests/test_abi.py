@@ -66,6 +66,7 @@ def test_workspace_size_formula(ep_size, E, K, H, C, dt):
     ((2, 8, 2, 12, 16, 0), "16 bytes"),
     ((2, 8, 2, 8, 16, 1), "16 bytes"),
     ((2, 8, 2, 256, -1, 0), "max_tokens_per_rank"),
+    ((64, 64, 2, 256, (1 << 24) + 1, 0), "2^30"),
     ((2, 8, 2, 256, 16, 7), "dtype"),
 ])
 def test_workspace_size_rejects(args, frag):
