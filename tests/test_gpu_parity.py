@@ -75,6 +75,10 @@ BASE = workloads.EpWorkload(name="edge", ep_size=4, num_experts=16, top_k=4, hid
     dict(dtype="fp32", hidden=264),                        # fp32 payload (1056-byte rows)
     dict(dtype="bf16", scales=True, scale_cols_override=7),  # odd scale width
     dict(dtype="fp8_e4m3", hidden=512, scales=True, scale_cols_override=16),  # 32-column groups
+    dict(dtype="fp32", hidden=16384, capacity=3, counts=("uniform", 0, 3)),  # 64 KB rows: 16 chunks
+    dict(ep_size=64, num_experts=128, top_k=32, capacity=2, counts=("full",)),  # widest fan-out
+    dict(ep_size=64, num_experts=64, top_k=32, capacity=2, counts=("full",), ids="uniform_dups",
+         dropped_ranks=tuple(range(0, 64, 3))),
     dict(hidden=8),                                        # one 16-byte vector per row
     dict(hidden=264),                                      # combine: 33 vectors, ragged block
 ])
