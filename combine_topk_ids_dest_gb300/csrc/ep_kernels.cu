@@ -1,30 +1,34 @@
 // ep_kernels.cu -- sm_103a kernels of rank-major MoE EP dispatch/combine with
 // every EP rank a virtual rank in this GPU's memory.
 //
-// dispatch_kernel (one warp per source slot s*T+t, grid-stride):
+// dispatch_kernel (one warp per (source slot s*T+t, column chunk of its
+// hidden row) work item, grid-stride):
+//   payload   -- the item's chunk of the hidden row is read once with 16-byte
+//                non-caching loads, issued first so they overlap the routing,
+//                and stored to every routed rank's row s*T+t.
 //   routing   -- lane k reads expert id k; the owners' bits are OR-reduced
 //                across the warp (two 32-bit halves for up to 64 ranks) and
 //                ANDed with active_rank_mask (page "flashinfer.moe_ep.
 //                NVLinkOneSidedAlltoAll", dispatch(): a masked-off rank
-//                receives nothing). The bit set is kept for combine.
-//   id plane  -- the slot's id row in every destination rank: the token's ids
-//                where it is routed, invalid_expert_id elsewhere and on padding
-//                slots (same page, class description).
-//   payload   -- the hidden row is read once with 16-byte non-caching loads
-//                and stored to every routed rank's row s*T+t, followed by the
-//                scale and weight rows (same page, class description: one
+//                receives nothing). The slot's first chunk keeps the bit set
+//                for combine.
+//   id plane  -- the slot's first chunk writes the slot's id row in every
+//                destination rank: the token's ids where it is routed,
+//                invalid_expert_id elsewhere and on padding slots (same page,
+//                class description), then the scale and weight rows (one
 //                dispatch carries all four payloads).
 //
-// combine_kernel (one thread per 16-byte column vector of one output row):
+// combine_kernel (each thread owns 4 16-byte column vectors of one live
+// token's output row):
 //   reads the row's slot in each routed rank's combine input in ascending
-//   rank order (loads of up to 8 ranks in flight before their adds), adds in
-//   fp32 from +0.0 and rounds once to bf16 (page "flashinfer.moe_ep.
+//   rank order, two ranks' loads in flight before their adds, adds in fp32
+//   from +0.0 and rounds once to bf16 (page "flashinfer.moe_ep.
 //   MoEEpCommunication", combine(): per token, the ranks' expert outputs are
 //   added up).
 //
 // Nothing here is a dense contraction; both kernels are bound by HBM
 // bandwidth, so the design is about coalesced 16-byte accesses and enough
-// bytes in flight per SM.
+// bytes in flight per SM. Launch shapes come from sweeps on GB300.
 #include "ep_internal.h"
 
 namespace epk {
@@ -44,25 +48,19 @@ namespace {
 #define EP_COMBINE_MAX_THREADS 256
 #endif
 #ifndef EP_COMBINE_VPT
-#define EP_COMBINE_VPT 4  // 16-byte column vectors per combine thread
+#define EP_COMBINE_VPT 4
 #endif
-#ifndef EP_DISPATCH_STORE_HINT
-#define EP_DISPATCH_STORE_HINT 0  // 0 plain, 1 .cs (evict-first), 2 .L1::no_allocate
-#endif
-#ifndef EP_COMBINE_L2_PREFETCH
-#define EP_COMBINE_L2_PREFETCH 0  // 1: .L2::256B on the combine's row loads
-#endif
-
-constexpr unsigned kFull = 0xffffffffu;
-constexpr int kDispatchThreads = EP_DISPATCH_THREADS;  // one warp per slot
-constexpr int kDispatchVecPerLane = EP_DISPATCH_VEC_PER_LANE;  // 16-byte vectors per lane per chunk
-constexpr int kDispatchBlocksPerSm = EP_DISPATCH_BLOCKS_PER_SM;  // grid cap, in blocks per SM
-constexpr int kCombineMaxThreads = EP_COMBINE_MAX_THREADS;
-constexpr int kCombineVpt = EP_COMBINE_VPT;
 #ifndef EP_COMBINE_BATCH
 #define EP_COMBINE_BATCH 2
 #endif
-constexpr int kCombineBatch = EP_COMBINE_BATCH;  // rank rows loaded before their adds
+
+constexpr unsigned kFull = 0xffffffffu;
+constexpr int kDispatchThreads = EP_DISPATCH_THREADS;          // one warp per work item
+constexpr int kDispatchVecPerLane = EP_DISPATCH_VEC_PER_LANE;  // 16-byte vectors per lane per chunk
+constexpr int kDispatchBlocksPerSm = EP_DISPATCH_BLOCKS_PER_SM;  // grid cap, in blocks per SM
+constexpr int kCombineMaxThreads = EP_COMBINE_MAX_THREADS;
+constexpr int kCombineVpt = EP_COMBINE_VPT;      // 16-byte column vectors per combine thread
+constexpr int kCombineBatch = EP_COMBINE_BATCH;  // ranks whose rows are loaded before their adds
 
 __device__ __forceinline__ uint4 ld_stream(const void *p)
 {
@@ -71,34 +69,6 @@ __device__ __forceinline__ uint4 ld_stream(const void *p)
         : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
         : "l"(p));
     return v;
-}
-
-__device__ __forceinline__ uint4 ld_rows(const void *p)
-{
-#if EP_COMBINE_L2_PREFETCH
-    uint4 v;
-    asm("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
-        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-        : "l"(p));
-    return v;
-#else
-    return ld_stream(p);
-#endif
-}
-
-__device__ __forceinline__ void st_row(uint4 *p, const uint4 &v)
-{
-#if EP_DISPATCH_STORE_HINT == 1
-    asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
-                 "r"(v.w)
-                 : "memory");
-#elif EP_DISPATCH_STORE_HINT == 2
-    asm volatile("st.global.L1::no_allocate.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
-                 "r"(v.z), "r"(v.w)
-                 : "memory");
-#else
-    *p = v;
-#endif
 }
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -234,7 +204,7 @@ __global__ void __launch_bounds__(kDispatchThreads)
             for (int j = 0; j < kDispatchVecPerLane; ++j) {
                 const int idx = c0 + j * 32 + lane;
                 if (idx < nvec)
-                    st_row(dst + idx, v[j]);
+                    dst[idx] = v[j];
             }
         }
         if (chunk != 0)
@@ -311,7 +281,7 @@ __global__ void __launch_bounds__(kCombineMaxThreads)
                     for (int j = 0; j < kCombineVpt; ++j) {
                         const int v = v0 + j * nthr;
                         if (v < nvec)
-                            x[r][j] = ld_rows(base + 16 * (long long)v);
+                            x[r][j] = ld_stream(base + 16 * (long long)v);
                     }
                     nb = r + 1;
                 }

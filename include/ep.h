@@ -218,8 +218,12 @@ ep_status ep_get_combine_input_buffer(ep_handle *h, int rank, void **out);
 ep_status ep_combine(ep_handle *h, const void *const *expert_output, void *const *output,
                      uint64_t active_rank_mask, void *stream);
 
-/* Frees the handle and (if ep_create allocated it) its workspace after
- * synchronising the device. NULL is a no-op (MoEEpCommunication.destroy). */
+/* Frees the handle and, when the library allocated the workspace (ep_create,
+ * or ep_create_ex with workspace NULL), that workspace: cudaFree waits for
+ * work using it. With a caller-owned workspace nothing is synchronised:
+ * finish the streams that used it before reusing or freeing that memory.
+ * NULL is a no-op; the Python binding makes repeated destroy() calls no-ops
+ * (MoEEpCommunication.destroy). */
 ep_status ep_destroy(ep_handle *h);
 
 /* Bit set of the listed ranks, for active_rank_mask; ranks outside [0, 64)
