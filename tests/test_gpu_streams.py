@@ -1,0 +1,87 @@
+"""Independent handles on independent streams: two communicators with
+different geometries run dispatch and combine concurrently on two non-default
+streams; each must match the oracle (no shared state on the main path). Also
+the binding's argument checks for tensors of the wrong kind."""
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from combine_topk_ids_dest_gb300 import EpComm
+from ep_testutil import EO_SEED, INV, bf16_bits, oracle_round, raw_bytes, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def test_two_handles_on_two_streams(cuda_device):
+    wls = [workloads.EpWorkload(name="sa", ep_size=8, num_experts=32, top_k=4, hidden=1024, dtype="bf16",
+                                capacity=64, runtime_max=None, counts=("uniform", 0, 64), seed=71),
+           workloads.EpWorkload(name="sb", ep_size=16, num_experts=64, top_k=8, hidden=512,
+                                dtype="fp8_e4m3", scales=True, capacity=48, runtime_max=40,
+                                counts=("uniform", 0, 40), dropped_ranks=(2, 7), seed=72)]
+    inps = [workloads.make_inputs(wl) for wl in wls]
+    comms = [EpComm(wl.ep_size, wl.num_experts, wl.top_k, wl.hidden, wl.capacity, dtype=wl.torch_dtype,
+                    enable_rank_mask=wl.enable_rank_mask, device=cuda_device) for wl in wls]
+    streams = [torch.cuda.Stream(cuda_device) for _ in wls]
+    try:
+        dev_in = [(to_dev(i.hidden, cuda_device), to_dev(i.topk_ids, cuda_device),
+                   to_dev(i.topk_weights, cuda_device), to_dev(i.scale, cuda_device)) for i in inps]
+        eos = []
+        for wl in wls:
+            rows = torch.arange(wl.ep_size * wl.tokens_per_rank)
+            eos.append([workloads.expert_output_rows(EO_SEED, d, rows, wl.hidden).to(cuda_device)
+                        for d in range(wl.ep_size)])
+        torch.cuda.synchronize(cuda_device)
+        results, outs = [], []
+        for _ in range(3):  # interleave the two handles' calls on their streams
+            results, outs = [None, None], [None, None]
+            for i, (wl, inp, comm, st) in enumerate(zip(wls, inps, comms, streams)):
+                with torch.cuda.stream(st):
+                    h, ids, w, sc = dev_in[i]
+                    mask = inp.active_rank_mask if wl.enable_rank_mask else None
+                    results[i] = comm.dispatch(h, ids, w, hidden_states_scale=sc,
+                                               runtime_max_tokens_per_rank=wl.runtime_max,
+                                               active_rank_mask=mask)
+            for i, (wl, inp, comm, st) in enumerate(zip(wls, inps, comms, streams)):
+                with torch.cuda.stream(st):
+                    mask = inp.active_rank_mask if wl.enable_rank_mask else None
+                    outs[i] = comm.combine(eos[i], active_rank_mask=mask)
+        torch.cuda.synchronize(cuda_device)
+        for i, inp in enumerate(inps):
+            disp, out = oracle_round(inp)
+            res = results[i]
+            for d in range(inp.wl.ep_size):
+                np.testing.assert_array_equal(res.topk_ids[d].cpu().numpy(), disp.recv_ids[d])
+                valid = (disp.recv_ids[d] != INV).any(axis=1)
+                np.testing.assert_array_equal(raw_bytes(res.hidden_states[d].cpu())[valid],
+                                              disp.recv_hidden[d][valid])
+            for s in range(inp.wl.ep_size):
+                np.testing.assert_array_equal(bf16_bits(outs[i][s].cpu()), out[s])
+    finally:
+        for c in comms:
+            c.destroy()
+
+
+def test_binding_rejects_wrong_tensors(cuda_device):
+    comm = EpComm(2, 4, 2, 64, 8, device=cuda_device)
+    try:
+        ids = [torch.zeros(3, 2, dtype=torch.int32, device=cuda_device)] * 2
+        good = [torch.zeros(3, 64, dtype=torch.bfloat16, device=cuda_device)] * 2
+        bad_cases = [
+            [torch.zeros(3, 64, dtype=torch.float16, device=cuda_device)] * 2,  # wrong dtype
+            [torch.zeros(3, 64, dtype=torch.bfloat16)] * 2,                     # on the CPU
+            [torch.zeros(64, 3, dtype=torch.bfloat16, device=cuda_device).t()] * 2,  # not contiguous
+            [torch.zeros(3, 32, dtype=torch.bfloat16, device=cuda_device)] * 2,  # wrong width
+            good[:1],                                                          # one rank missing
+        ]
+        for hid in bad_cases:
+            with pytest.raises(ValueError):
+                comm.dispatch(hid, ids)
+        with pytest.raises(ValueError):
+            comm.dispatch(good, [torch.zeros(3, 2, dtype=torch.int64, device=cuda_device)] * 2)
+        comm.dispatch(good, ids)  # the handle is still usable
+        with pytest.raises(ValueError):
+            comm.combine([torch.zeros(16, 64, dtype=torch.float32, device=cuda_device)] * 2)
+        comm.combine()
+    finally:
+        comm.destroy()
