@@ -72,6 +72,12 @@ def lib() -> ctypes.CDLL:
             L.oracle_identity_expert.argtypes = [i32, i32, i32, i32, i32, i32, i32,
                                                  P, P, P, P, P]
             L.oracle_identity_expert.restype = i32
+            L.oracle_f16_to_f32.argtypes = [ctypes.c_uint16]
+            L.oracle_f16_to_f32.restype = ctypes.c_float
+            L.oracle_f32_to_f16_rne.argtypes = [ctypes.c_float]
+            L.oracle_f32_to_f16_rne.restype = ctypes.c_uint16
+            L.oracle_combine_typed.argtypes = [i32, i32, i32, i32, i32, i32, u64, P, P, i32, P, P]
+            L.oracle_combine_typed.restype = i32
             L.oracle_eplb_gather.argtypes = [i32, i32, P, P]
             L.oracle_eplb_gather.restype = i32
             _lib = L
@@ -126,6 +132,16 @@ def f32_bits_to_bf16(bits: int) -> int:
     """f32_to_bf16 for an exact binary32 bit pattern (NaNs and -0 included)."""
     f = np.array([bits], dtype=np.uint32).view(np.float32)[0]
     return int(lib().oracle_f32_to_bf16_rne(ctypes.c_float(f)))
+
+
+def f16_to_f32(bits: int) -> float:
+    return float(lib().oracle_f16_to_f32(int(bits) & 0xFFFF))
+
+
+def f32_bits_to_f16(bits: int) -> int:
+    """binary32 bit pattern -> binary16 bits, round to nearest even."""
+    f = np.array([bits], dtype=np.uint32).view(np.float32)[0]
+    return int(lib().oracle_f32_to_f16_rne(ctypes.c_float(f)))
 
 
 def e4m3_to_f32(code: int) -> float:
@@ -260,4 +276,28 @@ def eplb_gather(local: Sequence) -> np.ndarray:
     p_loc, k = _ptrs(arrs)
     if lib().oracle_eplb_gather(len(arrs), nbytes, _voidp(p_loc), out.ctypes.data) != 0:
         raise ValueError("oracle_eplb_gather: inconsistent sizes")
+    return out
+
+
+COMBINE_DTYPES = {"bf16": (0, np.uint16), "fp16": (2, np.uint16), "fp32": (3, np.float32)}
+
+
+def combine_typed(ep_size: int, num_experts: int, top_k: int, hidden: int, tokens_per_rank: int,
+                  num_tokens: Sequence[int], topk_ids: Sequence, expert_output: Sequence, dtype: str, *,
+                  mask_enabled: bool = False, active_rank_mask: int = (1 << 64) - 1) -> List[np.ndarray]:
+    """combine() with expert outputs and results stored as ``dtype`` ("bf16",
+    "fp16" or "fp32"); returns raw bits (uint16) or float32 arrays [n_s, hidden]."""
+    code, npt = COMBINE_DTYPES[dtype]
+    counts = np.ascontiguousarray(np.asarray(num_tokens, dtype=np.int32))
+    ids = [_np(i, np.int32) for i in topk_ids]
+    eo = [np.ascontiguousarray(_np(e)).view(npt) for e in expert_output]
+    out = [np.zeros((int(n), hidden), npt) for n in counts]
+    p_ids, k1 = _ptrs(ids)
+    p_eo, k2 = _ptrs(eo)
+    p_out, k3 = _ptrs(out)
+    rc = lib().oracle_combine_typed(ep_size, num_experts, top_k, hidden, tokens_per_rank,
+                                    int(bool(mask_enabled)), active_rank_mask & ((1 << 64) - 1),
+                                    counts.ctypes.data, _voidp(p_ids), code, _voidp(p_eo), _voidp(p_out))
+    if rc != 0:
+        raise ValueError("oracle_combine_typed: inconsistent sizes")
     return out

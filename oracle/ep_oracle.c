@@ -96,6 +96,76 @@ float oracle_e4m3_to_f32(uint8_t v)
     return sign ? -mag : mag;
 }
 
+/* IEEE 754 binary16: 1 sign bit, 5 exponent bits with bias 15, 10 mantissa
+ * bits. Exponent field 0 is subnormal (m * 2^-24), 31 is infinity (m = 0)
+ * or NaN. Widening to binary32 is exact. */
+float oracle_f16_to_f32(uint16_t v)
+{
+    int sign = (v >> 15) & 1;
+    int e = (v >> 10) & 0x1F;
+    int m = v & 0x3FF;
+    float mag;
+    if (e == 0x1F) {
+        uint32_t bits = m ? 0x7FC00000u : 0x7F800000u;
+        memcpy(&mag, &bits, sizeof mag);
+    } else if (e == 0) {
+        mag = (float)m;
+        for (int i = 0; i < 24; ++i) mag = mag / 2.0f;
+    } else {
+        mag = 1.0f + (float)m / 1024.0f;
+        for (int i = 15; i < e; ++i) mag = mag * 2.0f;
+        for (int i = e; i < 15; ++i) mag = mag / 2.0f;
+    }
+    return sign ? -mag : mag;
+}
+
+/* binary32 -> binary16, round to nearest, ties to even. The binary32 value
+ * is (2^23 + mantissa) * 2^(e-23) for a normal input; it is cut to the
+ * binary16 grid (2^(e-10) for normal results, 2^-24 for subnormal ones) and
+ * the dropped bits decide the rounding. Results past the largest finite
+ * binary16 (65504) become infinity; binary32 subnormals are far below half
+ * the smallest binary16 subnormal and become signed zero. NaN becomes the
+ * quiet NaN with the sign kept. */
+uint16_t oracle_f32_to_f16_rne(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    uint16_t sign = (uint16_t)((u >> 16) & 0x8000u);
+    int exp = (int)((u >> 23) & 0xFFu);
+    uint32_t man = u & 0x7FFFFFu;
+    if (exp == 0xFF)
+        return (uint16_t)(sign | (man ? 0x7E00u : 0x7C00u));
+    if (exp == 0)
+        return sign;
+    int e = exp - 127;
+    uint32_t full = (1u << 23) | man;  /* 24 significant bits */
+    if (e > 15)
+        return (uint16_t)(sign | 0x7C00u);
+    int shift;     /* dropped low bits of `full` */
+    int base_exp;  /* biased exponent field before any carry */
+    if (e >= -14) {
+        shift = 13;
+        base_exp = e + 15;
+    } else {
+        shift = 13 + (-14 - e);  /* subnormal: grid of 2^-24 */
+        base_exp = 0;
+        if (shift > 24 + 1)
+            return sign; /* below half of the smallest subnormal */
+    }
+    uint32_t keep = full >> shift;
+    uint32_t rem = full & ((1u << shift) - 1u);
+    uint32_t half = 1u << (shift - 1);
+    if (rem > half || (rem == half && (keep & 1u)))
+        keep += 1u;
+    if (base_exp == 0)
+        return (uint16_t)(sign | keep); /* keep == 0x400 is the smallest normal */
+    /* normal: keep holds the implicit bit at 0x400; a carry to 0x800 steps the exponent */
+    uint32_t field = ((uint32_t)base_exp << 10) + (keep - 0x400u);
+    if (field >= 0x7C00u)
+        return (uint16_t)(sign | 0x7C00u);
+    return (uint16_t)(sign | field);
+}
+
 /* ---- routing ------------------------------------------------------------ */
 
 /* Does the token with top-k id row `ids` go to rank d? Yes when rank d is
@@ -210,6 +280,53 @@ int oracle_combine(int ep_size, int num_experts, int top_k, int hidden, int toke
                     acc = acc + oracle_bf16_to_f32(expert_output[d][r * hidden + h]);
                 }
                 out[s][(long)t * hidden + h] = oracle_f32_to_bf16_rne(acc);
+            }
+        }
+    }
+    return 0;
+}
+
+/* The same combine for expert outputs stored as bf16 (dtype 0), binary16
+ * (dtype 2) or binary32 (dtype 3): each element is widened to fp32, the
+ * routed ranks are added in ascending order from +0.0 in fp32, and the sum
+ * is rounded once to the same storage type (not rounded for binary32). */
+int oracle_combine_typed(int ep_size, int num_experts, int top_k, int hidden, int tokens_per_rank,
+                         int mask_enabled, uint64_t active_rank_mask, const int32_t *num_tokens,
+                         const int32_t *const *topk_ids, int dtype, const void *const *expert_output,
+                         void *const *out)
+{
+    if (check_geometry(ep_size, num_experts, top_k, tokens_per_rank, num_tokens))
+        return -1;
+    if (dtype != 0 && dtype != 2 && dtype != 3)
+        return -1;
+    const int T = tokens_per_rank;
+    for (int s = 0; s < ep_size; ++s) {
+        for (int t = 0; t < num_tokens[s]; ++t) {
+            long r = (long)s * T + t;
+            const int32_t *ids = topk_ids[s] + (long)t * top_k;
+            for (int h = 0; h < hidden; ++h) {
+                float acc = 0.0f;
+                for (int d = 0; d < ep_size; ++d) {
+                    if (!oracle_routed_to(ids, top_k, num_experts, ep_size, d, mask_enabled,
+                                          active_rank_mask))
+                        continue;
+                    long i = r * hidden + h;
+                    float x;
+                    if (dtype == 0)
+                        x = oracle_bf16_to_f32(((const uint16_t *)expert_output[d])[i]);
+                    else if (dtype == 2)
+                        x = oracle_f16_to_f32(((const uint16_t *)expert_output[d])[i]);
+                    else
+                        x = ((const float *)expert_output[d])[i];
+                    acc = acc + x;
+                }
+                long o = (long)t * hidden + h;
+                if (dtype == 0)
+                    ((uint16_t *)out[s])[o] = oracle_f32_to_bf16_rne(acc);
+                else if (dtype == 2)
+                    ((uint16_t *)out[s])[o] = oracle_f32_to_f16_rne(acc);
+                else
+                    ((float *)out[s])[o] = acc;
             }
         }
     }

@@ -104,3 +104,50 @@ def test_e4m3_closed_forms(code, value):
 def test_e4m3_nan_codes():
     assert math.isnan(oracle.e4m3_to_f32(0x7F))
     assert math.isnan(oracle.e4m3_to_f32(0xFF))
+
+
+def test_f16_widen_all_patterns():
+    bits = torch.arange(0, 1 << 16, dtype=torch.int32).to(torch.int16)
+    ref = bits.view(torch.float16).to(torch.float32).numpy()
+    for b in range(1 << 16):
+        got = oracle.f16_to_f32(b)
+        r = float(ref[b])
+        if math.isnan(r):
+            assert math.isnan(got), hex(b)
+        else:
+            assert struct.pack("<f", got) == struct.pack("<f", r), hex(b)
+
+
+@pytest.mark.parametrize("x,expected", [
+    (1.0, 0x3C00), (-2.0, 0xC000), (65504.0, 0x7BFF),
+    (65519.0, 0x7BFF),                  # below the midpoint to 65536: stays at the largest finite
+    (65520.0, 0x7C00),                  # the midpoint rounds to even, i.e. to infinity
+    (2.0 ** -24, 0x0001),               # smallest subnormal
+    (2.0 ** -25, 0x0000),               # exactly half of it: ties to even (zero)
+    (3 * 2.0 ** -26, 0x0001),           # above half
+    (2.0 ** -14, 0x0400),               # smallest normal
+    (1.0 + 2.0 ** -11, 0x3C00),         # midpoint, 1.0 is even
+    (1.0 + 3 * 2.0 ** -11, 0x3C02),     # midpoint between 0x3C01 and 0x3C02 (even)
+    (0.0, 0x0000), (-0.0, 0x8000), (float("inf"), 0x7C00), (float("-inf"), 0xFC00),
+])
+def test_f16_rne_closed_forms(x, expected):
+    assert oracle.f32_bits_to_f16(int(np.array([x], np.float32).view(np.uint32)[0])) == expected
+
+
+def test_f16_rne_matches_torch_on_random_tie_and_subnormal_patterns():
+    rng = np.random.default_rng(2)
+    pats = rng.integers(0, 1 << 32, size=4000, dtype=np.uint64).astype(np.uint32)
+    # exponents around the binary16 range, including its subnormals and overflow
+    exps = rng.integers(127 - 27, 127 + 17, size=6000, dtype=np.uint64).astype(np.uint32)
+    mans = rng.integers(0, 1 << 23, size=6000, dtype=np.uint64).astype(np.uint32)
+    sgn = rng.integers(0, 2, size=6000, dtype=np.uint64).astype(np.uint32) << 31
+    near = sgn | (exps << 23) | mans
+    ties = sgn[:3000] | (exps[:3000] << 23) | (mans[:3000] & ~np.uint32(0x1FFF)) | np.uint32(0x1000)
+    allp = np.concatenate([pats, near, ties])
+    f = allp.view(np.float32)
+    ref = torch.from_numpy(f.copy()).to(torch.float16).view(torch.int16).numpy().view(np.uint16)
+    for i in range(len(allp)):
+        if np.isnan(f[i]):
+            assert (oracle.f32_bits_to_f16(int(allp[i])) & 0x7C00) == 0x7C00
+            continue
+        assert oracle.f32_bits_to_f16(int(allp[i])) == int(ref[i]), hex(int(allp[i]))

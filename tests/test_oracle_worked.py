@@ -82,3 +82,30 @@ def test_combine_rounding_cases():
         eo = [np.full((ep * T, H), _hex(v), np.uint16) for v in case["eo"]]
         out = oracle.combine(ep, c["num_experts"], c["top_k"], H, T, counts, ids, eo)
         assert int(out[0][0, 0]) == _hex(case["expected"]), case["what"]
+
+
+def test_combine_rounding_cases_f16_f32():
+    g = _load("combine_rounding_f16_f32.json")
+    c = g["config"]
+    ep, T, H = c["ep_size"], c["tokens_per_rank"], c["hidden"]
+    ids = [np.array([g["topk_ids"]], np.int32)] + [np.zeros((0, c["top_k"]), np.int32)] * (ep - 1)
+    counts = [1] + [0] * (ep - 1)
+    for case in g["cases"]:
+        npt = np.uint32 if case["dtype"] == "fp32" else np.uint16
+        eo = [np.full((ep * T, H), _hex(v), npt) for v in case["eo"]]
+        out = oracle.combine_typed(ep, c["num_experts"], c["top_k"], H, T, counts, ids, eo, case["dtype"])
+        got = int(np.asarray(out[0]).view(npt)[0, 0])
+        assert got == _hex(case["expected"]), case["what"]
+
+
+def test_combine_typed_bf16_equals_combine():
+    g = _load("combine_rounding.json")
+    c = g["config"]
+    ep, T, H = c["ep_size"], c["tokens_per_rank"], c["hidden"]
+    ids = [np.array([g["topk_ids"]], np.int32)] + [np.zeros((0, c["top_k"]), np.int32)] * (ep - 1)
+    counts = [1] + [0] * (ep - 1)
+    for case in g["cases"]:
+        eo = [np.full((ep * T, H), _hex(v), np.uint16) for v in case["eo"]]
+        a = oracle.combine(ep, c["num_experts"], c["top_k"], H, T, counts, ids, eo)
+        b = oracle.combine_typed(ep, c["num_experts"], c["top_k"], H, T, counts, ids, eo, "bf16")
+        assert int(a[0][0, 0]) == int(b[0][0, 0]) == _hex(case["expected"])
