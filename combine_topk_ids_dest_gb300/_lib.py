@@ -53,7 +53,7 @@ class EpConfigC(ctypes.Structure):
     _fields_ = [("ep_size", ctypes.c_int), ("num_experts", ctypes.c_int), ("top_k", ctypes.c_int),
                 ("hidden", ctypes.c_int), ("max_tokens_per_rank", ctypes.c_int), ("dtype", ctypes.c_int),
                 ("enable_rank_mask", ctypes.c_int), ("scale_cols", ctypes.c_int),
-                ("eplb_stats_max_bytes", ctypes.c_int)]
+                ("eplb_stats_max_bytes", ctypes.c_int), ("combine_dtype", ctypes.c_int)]
 
 
 class EpDispatchArgsC(ctypes.Structure):

@@ -39,6 +39,7 @@ struct ep_handle {
     int ep, num_experts, top_k, hidden, capacity, experts_per_rank;
     ep_dtype dtype;
     int elem_bytes, row_bytes, scale_cols;
+    ep_dtype combine_dtype;
     int mask_enabled;
     int eplb_max_bytes;
     int device;
@@ -87,7 +88,7 @@ bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 uint64_t full_mask(int ep) { return ep >= 64 ? ~0ULL : ((1ULL << ep) - 1); }
 
 struct Layout {
-    int elem_bytes, row_bytes, scale_cols;
+    int elem_bytes, row_bytes, scale_cols, combine_elem;
     size_t off_hidden, off_scale, off_ids, off_weights, off_comb, off_mask, off_eplb, total;
     size_t st_hidden, st_scale, st_ids, st_weights, st_comb;
 };
@@ -118,6 +119,7 @@ ep_config default_config(int ep, int E, int K, int H, int C, ep_dtype dtype, int
     c.enable_rank_mask = enable_rank_mask;
     c.scale_cols = EP_SCALE_COLS_DEFAULT;
     c.eplb_stats_max_bytes = 0;
+    c.combine_dtype = EP_DTYPE_BF16;
     return c;
 }
 
@@ -139,8 +141,12 @@ ep_status plan(const ep_config *cfg, Layout *L)
         return fail(EP_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
     if (H < 1 || ((long long)H * elem) % 16 != 0)
         return fail(EP_ERR_INVALID_ARG, "hidden=%d: a row must be a positive multiple of 16 bytes", H);
-    if (H % 8 != 0)
-        return fail(EP_ERR_INVALID_ARG, "hidden=%d: the bf16 combine rows need hidden %% 8 == 0", H);
+    const ep_dtype cdt = cfg->combine_dtype;
+    if (cdt != EP_DTYPE_BF16 && cdt != EP_DTYPE_FP16 && cdt != EP_DTYPE_FP32)
+        return fail(EP_ERR_INVALID_ARG, "combine_dtype %d: use bf16, fp16 or fp32", (int)cdt);
+    const int ce = dtype_bytes(cdt);
+    if (((long long)H * ce) % 16 != 0)
+        return fail(EP_ERR_INVALID_ARG, "hidden=%d: the combine rows need hidden %% %d == 0", H, 16 / ce);
     if (C < 0)
         return fail(EP_ERR_INVALID_ARG, "max_tokens_per_rank=%d < 0", C);
     if ((long long)ep * C > (1LL << 30))  // slot and token indices are 32-bit in the kernels
@@ -163,7 +169,8 @@ ep_status plan(const ep_config *cfg, Layout *L)
     L->st_scale = align256(rows * L->scale_cols * sizeof(float));
     L->st_ids = align256(rows * K * sizeof(int32_t));
     L->st_weights = align256(rows * K * sizeof(float));
-    L->st_comb = align256(rows * H * 2);
+    L->combine_elem = ce;
+    L->st_comb = align256(rows * H * ce);
     size_t off = 0;
     L->off_hidden = off;
     off += L->st_hidden * ep;
@@ -234,6 +241,7 @@ ep_status make_handle(const ep_config *cfg, void *ws, size_t ws_bytes, bool own,
     h->scale_cols = L.scale_cols;
     h->mask_enabled = cfg->enable_rank_mask ? 1 : 0;
     h->eplb_max_bytes = cfg->eplb_stats_max_bytes;
+    h->combine_dtype = cfg->combine_dtype;
     h->device = dev;
     h->ws = static_cast<uint8_t *>(ws);
     h->ws_bytes = ws_bytes;
@@ -544,7 +552,7 @@ ep_status ep_combine(ep_handle *h, const void *const *expert_output, void *const
             p = h->ws + h->off_comb + (size_t)d * h->st_comb;
         else if (!aligned(p, 16))
             return fail(EP_ERR_INVALID_ARG, "expert_output[%d] is not 16-byte aligned", d);
-        a.eo[d] = static_cast<const uint16_t *>(p);
+        a.eo[d] = p;
     }
     a.token_offset[0] = 0;
     for (int s = 0; s < h->ep; ++s) {
@@ -554,12 +562,13 @@ ep_status ep_combine(ep_handle *h, const void *const *expert_output, void *const
             continue;
         if (!output[s] || !aligned(output[s], 16))
             return fail(EP_ERR_INVALID_ARG, "output[%d] is NULL or not 16-byte aligned", s);
-        a.out[s] = static_cast<uint16_t *>(output[s]);
+        a.out[s] = output[s];
     }
     a.route_mask = reinterpret_cast<const uint64_t *>(h->ws + h->off_mask);
     a.ep = h->ep;
     a.T = h->T;
     a.H = h->hidden;
+    a.ctype = (int)h->combine_dtype;
 
     nvtxRangePushA("ep_combine");
     cudaError_t ce = epk::launch_combine(a, static_cast<cudaStream_t>(stream));

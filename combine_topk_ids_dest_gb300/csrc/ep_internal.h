@@ -50,13 +50,14 @@ struct DispatchArgs {
 };
 
 struct CombineArgs {
-    const uint16_t *eo[kMaxEp];  // rank d's bf16 combine input, [ep*T, H]
-    uint16_t *out[kMaxEp];       // source rank s's bf16 output, [num_tokens[s], H]
+    const void *eo[kMaxEp];  // rank d's combine input, [ep*T, H] of ctype
+    void *out[kMaxEp];       // source rank s's output, [num_tokens[s], H] of ctype
     int num_tokens[kMaxEp];
     int token_offset[kMaxEp + 1];  // prefix sums of num_tokens: live token g of rank s has
                                    // token_offset[s] <= g < token_offset[s+1]
     const uint64_t *route_mask;    // [ep*T], written by the dispatch
     int ep, T, H;
+    int ctype;  // element type of eo/out: EP_DTYPE_BF16, EP_DTYPE_FP16 or EP_DTYPE_FP32
 };
 
 // Records `fmt` as the calling thread's ep_last_error() message (cleared for

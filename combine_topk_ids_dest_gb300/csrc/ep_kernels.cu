@@ -83,6 +83,79 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
     return r;
 }
 
+// binary16 halves of a 32-bit word, widened exactly (cvt.f32.f16).
+__device__ __forceinline__ float f16_lo(uint32_t w)
+{
+    float f;
+    asm("{ .reg .b16 lo, hi;\n mov.b32 {lo, hi}, %1;\n cvt.f32.f16 %0, lo; }" : "=f"(f) : "r"(w));
+    return f;
+}
+__device__ __forceinline__ float f16_hi(uint32_t w)
+{
+    float f;
+    asm("{ .reg .b16 lo, hi;\n mov.b32 {lo, hi}, %1;\n cvt.f32.f16 %0, hi; }" : "=f"(f) : "r"(w));
+    return f;
+}
+
+// Two fp32 -> packed binary16x2, round to nearest even (cvt.rn.f16x2.f32;
+// subnormal results kept). `lo` lands in the low half.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi)
+{
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Element codec of the combine, per storage type: how many elements a
+// 16-byte vector holds, how to widen them to fp32 and how to narrow the sums.
+template <int CT>
+struct CombineCodec;
+
+template <>
+struct CombineCodec<EP_DTYPE_BF16> {
+    static constexpr int kPerVec = 8;
+    __device__ static void widen(const uint4 &x, float *f)
+    {
+        f[0] = bf16_lo(x.x), f[1] = bf16_hi(x.x), f[2] = bf16_lo(x.y), f[3] = bf16_hi(x.y);
+        f[4] = bf16_lo(x.z), f[5] = bf16_hi(x.z), f[6] = bf16_lo(x.w), f[7] = bf16_hi(x.w);
+    }
+    __device__ static uint4 narrow(const float *a)
+    {
+        return make_uint4(pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]), pack_bf16x2(a[4], a[5]),
+                          pack_bf16x2(a[6], a[7]));
+    }
+};
+
+template <>
+struct CombineCodec<EP_DTYPE_FP16> {
+    static constexpr int kPerVec = 8;
+    __device__ static void widen(const uint4 &x, float *f)
+    {
+        f[0] = f16_lo(x.x), f[1] = f16_hi(x.x), f[2] = f16_lo(x.y), f[3] = f16_hi(x.y);
+        f[4] = f16_lo(x.z), f[5] = f16_hi(x.z), f[6] = f16_lo(x.w), f[7] = f16_hi(x.w);
+    }
+    __device__ static uint4 narrow(const float *a)
+    {
+        return make_uint4(pack_f16x2(a[0], a[1]), pack_f16x2(a[2], a[3]), pack_f16x2(a[4], a[5]),
+                          pack_f16x2(a[6], a[7]));
+    }
+};
+
+template <>
+struct CombineCodec<EP_DTYPE_FP32> {
+    static constexpr int kPerVec = 4;
+    __device__ static void widen(const uint4 &x, float *f)
+    {
+        f[0] = __uint_as_float(x.x), f[1] = __uint_as_float(x.y);
+        f[2] = __uint_as_float(x.z), f[3] = __uint_as_float(x.w);
+    }
+    __device__ static uint4 narrow(const float *a)
+    {
+        return make_uint4(__float_as_uint(a[0]), __float_as_uint(a[1]), __float_as_uint(a[2]),
+                          __float_as_uint(a[3]));
+    }
+};
+
 __global__ void __launch_bounds__(kDispatchThreads)
     dispatch_kernel(const __grid_constant__ DispatchArgs a)
 {
@@ -233,10 +306,14 @@ __global__ void __launch_bounds__(kDispatchThreads)
     }
 }
 
+template <int CT>
 __global__ void __launch_bounds__(kCombineMaxThreads)
     combine_kernel(const __grid_constant__ CombineArgs a, int blocks_per_row, long long n_blocks)
 {
-    const int nvec = a.H >> 3;  // 8 bf16 per 16-byte vector
+    using Codec = CombineCodec<CT>;
+    constexpr int kEpv = Codec::kPerVec;  // elements per 16-byte vector
+    const long long row_bytes = (long long)a.H * (16 / kEpv);
+    const int nvec = (int)(row_bytes >> 4);
     const int nthr = blockDim.x;
     for (long long b = blockIdx.x; b < n_blocks; b += gridDim.x) {
         // block -> (live token g, column chunk); g -> source rank s by binary
@@ -258,13 +335,13 @@ __global__ void __launch_bounds__(kCombineMaxThreads)
         if (v0 >= nvec)
             continue;
         const uint64_t m = a.route_mask[slot];
-        const long long row = (slot * a.H) * 2;  // byte offset of the slot's row in a rank's buffer
+        const long long row = slot * row_bytes;  // byte offset of the slot's row in a rank's buffer
 
-        float acc[kCombineVpt][8];
+        float acc[kCombineVpt][kEpv];
 #pragma unroll
         for (int j = 0; j < kCombineVpt; ++j)
 #pragma unroll
-            for (int e = 0; e < 8; ++e)
+            for (int e = 0; e < kEpv; ++e)
                 acc[j][e] = 0.0f;
 
         uint64_t mm = m;
@@ -276,7 +353,7 @@ __global__ void __launch_bounds__(kCombineMaxThreads)
                 if (mm) {
                     const int d = __ffsll((long long)mm) - 1;
                     mm &= mm - 1;
-                    const uint8_t *base = reinterpret_cast<const uint8_t *>(a.eo[d]) + row;
+                    const uint8_t *base = static_cast<const uint8_t *>(a.eo[d]) + row;
 #pragma unroll
                     for (int j = 0; j < kCombineVpt; ++j) {
                         const int v = v0 + j * nthr;
@@ -291,30 +368,21 @@ __global__ void __launch_bounds__(kCombineMaxThreads)
                 if (r < nb) {
 #pragma unroll
                     for (int j = 0; j < kCombineVpt; ++j) {
-                        acc[j][0] = __fadd_rn(acc[j][0], bf16_lo(x[r][j].x));
-                        acc[j][1] = __fadd_rn(acc[j][1], bf16_hi(x[r][j].x));
-                        acc[j][2] = __fadd_rn(acc[j][2], bf16_lo(x[r][j].y));
-                        acc[j][3] = __fadd_rn(acc[j][3], bf16_hi(x[r][j].y));
-                        acc[j][4] = __fadd_rn(acc[j][4], bf16_lo(x[r][j].z));
-                        acc[j][5] = __fadd_rn(acc[j][5], bf16_hi(x[r][j].z));
-                        acc[j][6] = __fadd_rn(acc[j][6], bf16_lo(x[r][j].w));
-                        acc[j][7] = __fadd_rn(acc[j][7], bf16_hi(x[r][j].w));
+                        float f[kEpv];
+                        Codec::widen(x[r][j], f);
+#pragma unroll
+                        for (int e = 0; e < kEpv; ++e)
+                            acc[j][e] = __fadd_rn(acc[j][e], f[e]);
                     }
                 }
             }
         }
-        uint4 *out = reinterpret_cast<uint4 *>(a.out[s] + (long long)t * a.H);
+        uint4 *out = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(a.out[s]) + (long long)t * row_bytes);
 #pragma unroll
         for (int j = 0; j < kCombineVpt; ++j) {
             const int v = v0 + j * nthr;
-            if (v < nvec) {
-                uint4 o;
-                o.x = pack_bf16x2(acc[j][0], acc[j][1]);
-                o.y = pack_bf16x2(acc[j][2], acc[j][3]);
-                o.z = pack_bf16x2(acc[j][4], acc[j][5]);
-                o.w = pack_bf16x2(acc[j][6], acc[j][7]);
-                out[v] = o;
-            }
+            if (v < nvec)
+                out[v] = Codec::narrow(acc[j]);
         }
     }
 }
@@ -371,7 +439,8 @@ cudaError_t launch_dispatch(const DispatchArgs &a, cudaStream_t stream)
 
 cudaError_t launch_combine(const CombineArgs &a, cudaStream_t stream)
 {
-    const int nvec = a.H >> 3;
+    const int elem = a.ctype == EP_DTYPE_FP32 ? 4 : 2;
+    const int nvec = (int)(((long long)a.H * elem) >> 4);
     const int threads = combine_threads(nvec);
     const int per_block = threads * kCombineVpt;
     const int bpr = (nvec + per_block - 1) / per_block;
@@ -381,7 +450,19 @@ cudaError_t launch_combine(const CombineArgs &a, cudaStream_t stream)
     long long grid = n_blocks;
     if (grid > (1LL << 30))
         grid = 1LL << 30;
-    combine_kernel<<<(unsigned)grid, threads, 0, stream>>>(a, bpr, n_blocks);
+    switch (a.ctype) {
+    case EP_DTYPE_BF16:
+        combine_kernel<EP_DTYPE_BF16><<<(unsigned)grid, threads, 0, stream>>>(a, bpr, n_blocks);
+        break;
+    case EP_DTYPE_FP16:
+        combine_kernel<EP_DTYPE_FP16><<<(unsigned)grid, threads, 0, stream>>>(a, bpr, n_blocks);
+        break;
+    case EP_DTYPE_FP32:
+        combine_kernel<EP_DTYPE_FP32><<<(unsigned)grid, threads, 0, stream>>>(a, bpr, n_blocks);
+        break;
+    default:
+        return cudaErrorInvalidValue;
+    }
     return cudaGetLastError();
 }
 

@@ -22,6 +22,7 @@ from ._lib import ALL_RANKS, EpError, check, ptr_array
 
 _DTYPES = {torch.bfloat16: _lib.EP_DTYPE_BF16, torch.float8_e4m3fn: _lib.EP_DTYPE_FP8_E4M3,
            torch.float16: _lib.EP_DTYPE_FP16, torch.float32: _lib.EP_DTYPE_FP32}
+_COMBINE_DTYPES = (torch.bfloat16, torch.float16, torch.float32)
 
 
 @dataclass
@@ -67,14 +68,16 @@ class EpComm:
     ``torch.float16`` or ``torch.float32``. ``scale_cols`` is the number of
     fp32 scales per row (default hidden/128 when that divides, else none).
     ``eplb_stats_max_bytes`` reserves room to all-gather that many bytes of
-    ``eplb_local_stats`` per rank. The workspace is allocated here with
-    torch, at capacity ``max_tokens_per_rank``.
+    ``eplb_local_stats`` per rank. ``combine_dtype`` (bf16, fp16 or fp32)
+    is the type of the expert outputs combine sums and of its results. The
+    workspace is allocated here with torch, at capacity
+    ``max_tokens_per_rank``.
     """
 
     def __init__(self, ep_size: int, num_experts: int, top_k: int, hidden: int,
                  max_tokens_per_rank: int, dtype: torch.dtype = torch.bfloat16,
                  enable_rank_mask: bool = False, device=None, scale_cols: Optional[int] = None,
-                 eplb_stats_max_bytes: int = 0):
+                 eplb_stats_max_bytes: int = 0, combine_dtype: torch.dtype = torch.bfloat16):
         self._L = _lib.load()
         if dtype not in _DTYPES:
             raise ValueError(f"dtype {dtype} not supported (bfloat16, float8_e4m3fn, float16, float32)")
@@ -88,9 +91,12 @@ class EpComm:
             scale_cols = self.hidden // _lib.EP_SCALE_GROUP if self.hidden % _lib.EP_SCALE_GROUP == 0 else 0
         self.scale_cols = int(scale_cols)
         self.eplb_stats_max_bytes = int(eplb_stats_max_bytes)
+        if combine_dtype not in _COMBINE_DTYPES:
+            raise ValueError(f"combine_dtype {combine_dtype} not supported (bfloat16, float16, float32)")
+        self.combine_dtype = combine_dtype
         cfg = _lib.EpConfigC(self.ep_size, self.num_experts, self.top_k, self.hidden,
                              self.max_tokens_per_rank, _DTYPES[dtype], int(self.enable_rank_mask),
-                             self.scale_cols, self.eplb_stats_max_bytes)
+                             self.scale_cols, self.eplb_stats_max_bytes, _DTYPES[combine_dtype])
         nbytes = ctypes.c_size_t(0)
         check(self._L.ep_workspace_size_ex(ctypes.byref(cfg), ctypes.byref(nbytes)))
         with torch.cuda.device(self.device):
@@ -222,12 +228,14 @@ class EpComm:
         return EpDispatchResult(T, hs, sc, ids, w, stats)
 
     # -- MoEEpCommunication.get_combine_input_buffer ------------------------
-    def get_combine_input_buffer(self, dtype: torch.dtype = torch.bfloat16, *, rank: Optional[int] = None):
-        """Rank ``rank``'s bf16 [ep_size*tokens_per_rank, hidden] combine input
-        (all ranks as a list when ``rank`` is None); None for other dtypes.
+    def get_combine_input_buffer(self, dtype: Optional[torch.dtype] = None, *,
+                                 rank: Optional[int] = None):
+        """Rank ``rank``'s [ep_size*tokens_per_rank, hidden] combine input of
+        the communicator's combine dtype (all ranks as a list when ``rank`` is
+        None); None when ``dtype`` names another type (no such buffer).
         Usable from a dispatch() until the combine() that follows it."""
         self._live()
-        if dtype != torch.bfloat16:
+        if dtype is not None and dtype != self.combine_dtype:
             return None
         ranks = range(self.ep_size) if rank is None else [int(rank)]
         out = []
@@ -238,7 +246,7 @@ class EpComm:
             v = self._views.get(key)
             if v is None:
                 v = self._views[key] = self._view(p.value, self.ep_size * self._T, self.hidden,
-                                                  torch.bfloat16)
+                                                  self.combine_dtype)
             out.append(v)
         return out if rank is None else out[0]
 
@@ -246,12 +254,13 @@ class EpComm:
     def combine(self, expert_output: Optional[Sequence[Optional[torch.Tensor]]] = None, *,
                 output: Optional[Sequence[torch.Tensor]] = None,
                 active_rank_mask=None) -> List[torch.Tensor]:
-        """Per source rank, bf16 [n_s, hidden]: the sum over the ranks each
-        token was routed to (ascending, fp32) of their expert_output rows.
+        """Per source rank, [n_s, hidden] of the combine dtype: the sum over
+        the ranks each token was routed to (ascending, fp32, one rounding) of
+        their expert_output rows.
 
-        ``expert_output[d]`` is rank d's bf16 [ep_size*tokens_per_rank, hidden]
-        (or [ep_size, tokens_per_rank, hidden]) tensor; None, or a None entry,
-        means the backend combine input buffer (no copy)."""
+        ``expert_output[d]`` is rank d's [ep_size*tokens_per_rank, hidden] (or
+        [ep_size, tokens_per_rank, hidden]) tensor of the combine dtype; None,
+        or a None entry, means the backend combine input buffer (no copy)."""
         self._live()
         ep, H = self.ep_size, self.hidden
         if self._counts is None:
@@ -266,18 +275,18 @@ class EpComm:
                 if e is None:
                     eo_ptrs.append(0)
                     continue
-                if e.dtype is not torch.bfloat16 or not e.is_cuda or e.get_device() != self._dev_index \
+                if e.dtype is not self.combine_dtype or not e.is_cuda or e.get_device() != self._dev_index \
                         or not e.is_contiguous() or e.numel() != rows * H or e.shape[-1] != H:
-                    raise ValueError(f"expert_output[{d}] must be contiguous bf16 [{rows}, {H}] on "
-                                     f"{self.device}")
+                    raise ValueError(f"expert_output[{d}] must be contiguous {self.combine_dtype} "
+                                     f"[{rows}, {H}] on {self.device}")
                 eo_ptrs.append(e.data_ptr())
         if output is None:
-            output = [torch.empty(n, H, dtype=torch.bfloat16, device=self.device) for n in self._counts]
+            output = [torch.empty(n, H, dtype=self.combine_dtype, device=self.device) for n in self._counts]
         else:
             if len(output) != ep:
                 raise ValueError(f"output needs {ep} per-rank tensors")
             for s in range(ep):
-                self._check_rank_tensor("output", output[s], s, self._counts[s], H, torch.bfloat16)
+                self._check_rank_tensor("output", output[s], s, self._counts[s], H, self.combine_dtype)
         with torch.cuda.device(self.device):
             check(self._L.ep_combine(self._h, ptr_array(eo_ptrs) if eo_ptrs is not None else None,
                                      ptr_array([o.data_ptr() for o in output]),

@@ -32,8 +32,9 @@
  *    hidden, scale and weight rows keep whatever they held.
  *  - the rank mask filters destinations only.
  *  - combine adds, per token, the rows of the ranks it was routed to, in
- *    ascending rank order, in fp32 from +0.0, and rounds once to bf16
- *    (round to nearest even). The result is bit-exact and deterministic.
+ *    ascending rank order, in fp32 from +0.0, and rounds once (round to
+ *    nearest even) to the combine dtype: bf16 by default, or fp16; fp32
+ *    results are not rounded. The result is bit-exact and deterministic.
  *
  * Errors are synchronous: each call checks its arguments and the handle's
  * state on the host before it launches anything, and returns a status;
@@ -105,6 +106,9 @@ typedef struct {
     int scale_cols;            /* fp32 scales per row: EP_SCALE_COLS_DEFAULT, 0 (none) or > 0 */
     int eplb_stats_max_bytes;  /* eplb_local_stats bytes per rank the handle can gather, a
                                   multiple of 4 (0: not supported) */
+    ep_dtype combine_dtype;    /* type of the expert outputs combine sums and of its results:
+                                  EP_DTYPE_BF16 (0, the default), EP_DTYPE_FP16 or EP_DTYPE_FP32;
+                                  hidden*elem_bytes of it must be a multiple of 16 */
 } ep_config;
 
 /* Everything one dispatch takes (ep_dispatch_ex); see ep_dispatch for the
@@ -197,8 +201,9 @@ ep_status ep_dispatch(ep_handle *h, const void *const *hidden, const float *cons
 ep_status ep_dispatch_ex(ep_handle *h, const ep_dispatch_args *args, void *stream,
                          ep_dispatch_result *out);
 
-/* Device pointer to rank `rank`'s backend-owned combine input: bf16
- * [ep_size*tokens_per_rank, hidden] of the pending dispatch. Passing it (or
+/* Device pointer to rank `rank`'s backend-owned combine input: [ep_size *
+ * tokens_per_rank, hidden] elements of the handle's combine dtype (bf16
+ * unless ep_config.combine_dtype says otherwise) for the pending dispatch. Passing it (or
  * NULL) to ep_combine avoids one copy. Valid between ep_dispatch and
  * ep_combine; EP_ERR_STATE outside (MoEEpCommunication.get_combine_input_buffer,
  * NVLinkOneSidedAlltoAll.get_combine_input_buffer). */
@@ -206,15 +211,16 @@ ep_status ep_get_combine_input_buffer(ep_handle *h, int rank, void **out);
 
 /* Combine of the pending dispatch (MoEEpCommunication.combine).
  *  expert_output   NULL = every rank's backend combine input buffer; else
- *                  expert_output[d] is rank d's bf16 [ep_size*tokens_per_rank,
- *                  hidden] device buffer (NULL entry = that rank's backend
- *                  buffer), 16-byte aligned; only routed rows are read.
- *  output[s]       device bf16 [num_tokens[s], hidden], 16-byte aligned,
- *                  caller-owned; may be NULL when num_tokens[s] == 0.
+ *                  expert_output[d] is rank d's [ep_size*tokens_per_rank, hidden]
+ *                  device buffer of the combine dtype (NULL entry = that rank's
+ *                  backend buffer), 16-byte aligned; only routed rows are read.
+ *  output[s]       device [num_tokens[s], hidden] of the combine dtype, 16-byte
+ *                  aligned, caller-owned; may be NULL when num_tokens[s] == 0.
  *  active_rank_mask  must equal the dispatch's (when masking is enabled).
- * output[s][t] = bf16( sum over routed ranks d ascending of expert_output[d]
- * [s*tokens_per_rank + t] ) with an fp32 accumulator from +0.0. A token
- * routed nowhere gets +0.0. Returns the handle to the idle state. */
+ * output[s][t] = round( sum over routed ranks d ascending of expert_output[d]
+ * [s*tokens_per_rank + t] ) with an fp32 accumulator from +0.0 and one
+ * round-to-nearest-even to the combine dtype (none for fp32). A token routed
+ * nowhere gets +0.0. Returns the handle to the idle state. */
 ep_status ep_combine(ep_handle *h, const void *const *expert_output, void *const *output,
                      uint64_t active_rank_mask, void *stream);
 

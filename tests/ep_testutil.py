@@ -29,6 +29,14 @@ def bf16_bits(t):
     return t.detach().contiguous().view(torch.int16).numpy().view(np.uint16)
 
 
+def out_bits(t):
+    """Raw bits of a bf16/fp16 (uint16) or fp32 (uint32) CPU tensor."""
+    t = t.detach().contiguous()
+    if t.dtype == torch.float32:
+        return t.view(torch.int32).numpy().view(np.uint32)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
 def small(wl, hidden=256, tokens=None):
     """The same EP geometry, id law and dtypes as ``wl`` with a short hidden
     row and few tokens per rank, so the oracle runs in well under a second."""
@@ -53,6 +61,9 @@ def to_dev(lst, device):
     return None if lst is None else [x.to(device) for x in lst]
 
 
+_CDT = {torch.bfloat16: "bf16", torch.float16: "fp16", torch.float32: "fp32"}
+
+
 def fill_expert_outputs(comm, T, device, seed=EO_SEED, special=False, caller=False):
     """Writes the stand-in expert outputs of every rank: into the backend
     combine-input buffers, or (caller=True) into fresh tensors it returns."""
@@ -61,7 +72,8 @@ def fill_expert_outputs(comm, T, device, seed=EO_SEED, special=False, caller=Fal
     rows = torch.arange(ep * T, device=device)
     outs = []
     for d in range(ep):
-        eo = workloads.expert_output_rows(seed, d, rows, H, device=device, special=special)
+        eo = workloads.expert_output_rows(seed, d, rows, H, device=device, special=special,
+                                          dtype=_CDT[comm.combine_dtype])
         if caller:
             outs.append(eo.contiguous())
         else:
@@ -78,7 +90,8 @@ def gpu_round(inp, device, special=False, caller_eo=False, comm=None, keep=False
     if own:
         comm = EpComm(wl.ep_size, wl.num_experts, wl.top_k, wl.hidden, wl.capacity, dtype=wl.torch_dtype,
                       enable_rank_mask=wl.enable_rank_mask, device=device,
-                      scale_cols=wl.scale_cols if wl.scales else None)
+                      scale_cols=wl.scale_cols if wl.scales else None,
+                      combine_dtype=wl.combine_torch_dtype)
     mask = inp.active_rank_mask if wl.enable_rank_mask else None
     res = comm.dispatch(to_dev(inp.hidden, device), to_dev(inp.topk_ids, device),
                         to_dev(inp.topk_weights, device),
@@ -95,7 +108,7 @@ def gpu_round(inp, device, special=False, caller_eo=False, comm=None, keep=False
         recv_scale=None if res.hidden_states_scale is None else
         [x.cpu().numpy() for x in res.hidden_states_scale],
         recv_weights=None if res.topk_weights is None else [x.cpu().numpy() for x in res.topk_weights],
-        out=[bf16_bits(o.cpu()) for o in out],
+        out=[out_bits(o.cpu()) for o in out],
     )
     if own and not keep:
         comm.destroy()
@@ -116,10 +129,16 @@ def oracle_round(inp, special=False):
                            mask_enabled=wl.enable_rank_mask, active_rank_mask=inp.active_rank_mask,
                            row_bytes=H * wl.elem_bytes, scale_cols=wl.scale_cols)
     rows = torch.arange(ep * T)
-    eo = [bf16_bits(workloads.expert_output_rows(EO_SEED, d, rows, H, special=special))
-          for d in range(ep)]
-    out = oracle.combine(ep, wl.num_experts, wl.top_k, H, T, inp.num_tokens, inp.topk_ids, eo,
-                         mask_enabled=wl.enable_rank_mask, active_rank_mask=inp.active_rank_mask)
+    eo = [out_bits(workloads.expert_output_rows(EO_SEED, d, rows, H, special=special,
+                                                dtype=wl.combine_dtype)) for d in range(ep)]
+    if wl.combine_dtype == "bf16":
+        out = oracle.combine(ep, wl.num_experts, wl.top_k, H, T, inp.num_tokens, inp.topk_ids, eo,
+                             mask_enabled=wl.enable_rank_mask, active_rank_mask=inp.active_rank_mask)
+    else:
+        out = oracle.combine_typed(ep, wl.num_experts, wl.top_k, H, T, inp.num_tokens, inp.topk_ids, eo,
+                                   wl.combine_dtype, mask_enabled=wl.enable_rank_mask,
+                                   active_rank_mask=inp.active_rank_mask)
+        out = [o.view(np.uint32) if o.dtype == np.float32 else o for o in out]
     return disp, out
 
 

@@ -108,7 +108,7 @@ def test_create_without_gpu_reports_error():
 
 def _size_ex(**kw):
     base = dict(ep_size=4, num_experts=8, top_k=2, hidden=256, max_tokens_per_rank=16, dtype=0,
-                enable_rank_mask=0, scale_cols=-1, eplb_stats_max_bytes=0)
+                enable_rank_mask=0, scale_cols=-1, eplb_stats_max_bytes=0, combine_dtype=0)
     base.update(kw)
     cfg = _lib.EpConfigC(*[base[f] for f, _ in _lib.EpConfigC._fields_])
     n = ctypes.c_size_t(0)
@@ -129,6 +129,25 @@ def test_workspace_size_ex_formula(dtype, elem, scale_cols, G, eplb):
     assert n == want
 
 
+@pytest.mark.parametrize("cdt,ce", [(0, 2), (2, 2), (3, 4)])
+def test_workspace_size_ex_combine_dtype(cdt, ce):
+    st, n = _size_ex(combine_dtype=cdt)
+    assert st == ep.EP_OK
+    rows = 4 * 16
+    want = 4 * (_align(rows * 256 * 2) + _align(rows * 2 * 4) + _align(rows * 2 * 4) * 2 +
+                _align(rows * 256 * ce)) + _align(rows * 8)
+    assert n == want
+
+
+def test_combine_dtype_rules():
+    st, _ = _size_ex(combine_dtype=1)  # fp8 is not a combine type
+    assert st == ep.EP_ERR_INVALID_ARG and b"combine_dtype" in _lib.load().ep_last_error()
+    st, _ = _size_ex(combine_dtype=3, dtype=3, hidden=12)  # 48-byte fp32 rows: fine
+    assert st == ep.EP_OK
+    st, _ = _size_ex(combine_dtype=2, dtype=3, hidden=12)  # 24-byte fp16 combine rows: not
+    assert st == ep.EP_ERR_INVALID_ARG and b"hidden % 8" in _lib.load().ep_last_error()
+
+
 def test_default_config_matches_plain_workspace_size():
     assert _size_ex() == _size(4, 8, 2, 256, 16, 0)
 
@@ -138,7 +157,7 @@ def test_default_config_matches_plain_workspace_size():
     (dict(eplb_stats_max_bytes=6), "eplb_stats_max_bytes"),
     (dict(eplb_stats_max_bytes=-4), "eplb_stats_max_bytes"),
     (dict(dtype=4), "dtype"),
-    (dict(dtype=3, hidden=12), "hidden % 8"),   # 48-byte fp32 rows, but combine needs 8 | hidden
+    (dict(dtype=3, hidden=12), "hidden % 8"),   # 48-byte fp32 rows, but a bf16 combine needs 8 | hidden
     (dict(dtype=1, hidden=24), "16 bytes"),     # 24-byte fp8 rows
 ])
 def test_workspace_size_ex_rejects(kw, frag):

@@ -36,8 +36,10 @@ def _case(seed):
     dropped = None
     if rng.random() < 0.4:
         dropped = tuple(r for r in range(ep) if rng.random() < 0.3)
+    cdt = rng.choice(["bf16", "bf16", "fp16", "fp32"])
     return workloads.EpWorkload(
         name=f"fuzz{seed}", ep_size=ep, num_experts=E, top_k=K, hidden=hidden, dtype=dtype,
+        combine_dtype=cdt,
         capacity=cap, runtime_max=rt, counts=counts, ids=ids, weights=rng.random() < 0.7,
         scales=scales, scale_cols_override=scale_cols, dropped_ranks=dropped, seed=seed), \
         rng.random() < 0.3

@@ -72,3 +72,32 @@ def test_combine_rounding_on_gpu(cuda_device):
             assert (got == int(case["expected"], 16)).all(), case["what"]
     finally:
         comm.destroy()
+
+
+@pytest.mark.parametrize("cdt", ["fp16", "fp32"])
+def test_combine_rounding_f16_f32_on_gpu(cuda_device, cdt):
+    from combine_topk_ids_dest_gb300 import EpComm
+    g = _load("combine_rounding_f16_f32.json")
+    c = g["config"]
+    ep, E, K, T = c["ep_size"], c["num_experts"], c["top_k"], c["tokens_per_rank"]
+    H = 8
+    tdt, idt = (torch.float16, torch.int16) if cdt == "fp16" else (torch.float32, torch.int32)
+    comm = EpComm(ep, E, K, H, T, device=cuda_device, combine_dtype=tdt)
+    try:
+        ids = [torch.tensor([g["topk_ids"]], dtype=torch.int32, device=cuda_device)] + \
+              [torch.zeros(0, K, dtype=torch.int32, device=cuda_device)] * (ep - 1)
+        hid = [torch.zeros(x.shape[0], H, dtype=torch.bfloat16, device=cuda_device) for x in ids]
+        for case in (x for x in g["cases"] if x["dtype"] == cdt):
+            comm.dispatch(hid, ids)
+            eo = []
+            for v in case["eo"]:
+                b = int(v, 16)
+                width = 16 if cdt == "fp16" else 32
+                if b >= 1 << (width - 1):
+                    b -= 1 << width
+                eo.append(torch.full((ep * T, H), b, dtype=idt, device=cuda_device).view(tdt))
+            out = comm.combine(eo)
+            got = out[0][0].view(idt).cpu().numpy().view(np.uint16 if cdt == "fp16" else np.uint32)
+            assert (got == int(case["expected"], 16)).all(), case["what"]
+    finally:
+        comm.destroy()

@@ -79,6 +79,10 @@ BASE = workloads.EpWorkload(name="edge", ep_size=4, num_experts=16, top_k=4, hid
     dict(ep_size=64, num_experts=128, top_k=32, capacity=2, counts=("full",)),  # widest fan-out
     dict(ep_size=64, num_experts=64, top_k=32, capacity=2, counts=("full",), ids="uniform_dups",
          dropped_ranks=tuple(range(0, 64, 3))),
+    dict(combine_dtype="fp16"),                            # fp16 expert outputs and results
+    dict(combine_dtype="fp32", hidden=264),                # fp32 combine, 1056-byte rows
+    dict(combine_dtype="fp32", dtype="fp8_e4m3", hidden=512, scales=True, dropped_ranks=(1,)),
+    dict(combine_dtype="fp16", hidden=4104, capacity=4, counts=("uniform", 0, 4)),  # ragged blocks
     dict(hidden=8),                                        # one 16-byte vector per row
     dict(hidden=264),                                      # combine: 33 vectors, ragged block
 ])
@@ -86,8 +90,9 @@ def test_edge_cases(cuda_device, variant):
     _check(BASE.replace(**variant), cuda_device)
 
 
-def test_subnormal_and_zero_expert_outputs(cuda_device):
-    _check(BASE.replace(hidden=512), cuda_device, special=True)
+@pytest.mark.parametrize("cdt", ["bf16", "fp16", "fp32"])
+def test_subnormal_and_zero_expert_outputs(cuda_device, cdt):
+    _check(BASE.replace(hidden=512, combine_dtype=cdt), cuda_device, special=True)
 
 
 def test_caller_owned_expert_outputs(cuda_device):

@@ -49,6 +49,7 @@ class EpWorkload:
     dropped_ranks: Optional[tuple] = None  # ranks left out of active_rank_mask
     seed: int = 0
     scale_cols_override: Optional[int] = None  # scale columns when not hidden/128
+    combine_dtype: str = "bf16"  # expert outputs / combine results: "bf16", "fp16" or "fp32"
 
     @property
     def tokens_per_rank(self) -> int:
@@ -66,6 +67,10 @@ class EpWorkload:
     def torch_dtype(self):
         return {"bf16": torch.bfloat16, "fp16": torch.float16, "fp8_e4m3": torch.float8_e4m3fn,
                 "fp32": torch.float32}[self.dtype]
+
+    @property
+    def combine_torch_dtype(self):
+        return {"bf16": torch.bfloat16, "fp16": torch.float16, "fp32": torch.float32}[self.combine_dtype]
 
     @property
     def scale_cols(self) -> int:
@@ -243,15 +248,18 @@ def _mix32(x: torch.Tensor) -> torch.Tensor:
 
 
 def expert_output_rows(seed: int, dest: int, rows: torch.Tensor, hidden: int,
-                       device=None, special: bool = False) -> torch.Tensor:
-    """bf16 [len(rows), hidden] stand-in expert output rows of rank ``dest``.
+                       device=None, special: bool = False, dtype: str = "bf16") -> torch.Tensor:
+    """[len(rows), hidden] stand-in expert output rows of rank ``dest``, as
+    bf16 (default), fp16 or fp32.
 
     Element (dest, row, h) is a pure function of its coordinates: sign and
-    7 mantissa bits from a 32-bit hash, biased exponent in [120, 134]
-    (magnitudes 2^-7 .. 2^8). With ``special`` the exponent range also covers
-    zeros, subnormals and tiny normals (biased exponent 0..3), to exercise the
-    fp32 accumulation without flush-to-zero.
+    mantissa bits from 32-bit hashes, exponent within 2^-7 .. 2^8 (bf16/fp32:
+    biased 120..134; fp16: biased 8..22). With ``special`` the exponent range
+    also covers zeros, subnormals and tiny normals (biased exponent 0..3), to
+    exercise the fp32 accumulation without flush-to-zero.
     """
+    if dtype != "bf16":
+        return _expert_output_rows_wide(seed, dest, rows, hidden, device, special, dtype)
     device = rows.device if device is None else device
     r = rows.to(device=device, dtype=torch.int64).view(-1, 1)
     h = torch.arange(hidden, device=device, dtype=torch.int64).view(1, -1)
@@ -268,3 +276,31 @@ def expert_output_rows(seed: int, dest: int, rows: torch.Tensor, hidden: int,
     bits = (sign << 15) | (ex << 7) | mant
     bits = torch.where(bits >= 0x8000, bits - 0x10000, bits)  # reinterpret as int16
     return bits.to(torch.int16).view(torch.bfloat16)
+
+
+def _expert_output_rows_wide(seed, dest, rows, hidden, device, special, dtype):
+    device = rows.device if device is None else device
+    r = rows.to(device=device, dtype=torch.int64).view(-1, 1)
+    h = torch.arange(hidden, device=device, dtype=torch.int64).view(1, -1)
+    key = (seed * 0x9E37 + dest * 0x3C6EF372 + r * 0x1B873593 + h * 0x27D4EB2F) & _M32
+    x = _mix32(key)
+    y = _mix32(x ^ 0x5BD1E995)
+    z = _mix32(y ^ 0x68E31DA4)
+    sign = (x >> 31) & 1
+    if dtype == "fp16":
+        mant = (x >> 8) & 0x3FF
+        ex = y % 19 if special else 8 + (y % 15)
+        if special:
+            ex = torch.where(ex < 4, ex, ex + 4)  # 0..3 or 8..22
+        bits = (sign << 15) | (ex << 10) | mant
+        bits = torch.where(bits >= 0x8000, bits - 0x10000, bits)
+        return bits.to(torch.int16).view(torch.float16)
+    if dtype == "fp32":
+        mant = (((x >> 8) & 0x7F) << 16) | (z & 0xFFFF)
+        ex = y % 19 if special else 120 + (y % 15)
+        if special:
+            ex = torch.where(ex < 4, ex, ex + 116)
+        bits = (sign << 31) | (ex << 23) | mant
+        bits = torch.where(bits >= (1 << 31), bits - (1 << 32), bits)
+        return bits.to(torch.int32).view(torch.float32)
+    raise ValueError(dtype)
