@@ -8,7 +8,6 @@ import ctypes
 import os
 import threading
 
-from . import build as _build
 
 EP_OK = 0
 EP_ERR_INVALID_ARG = 1
@@ -75,6 +74,7 @@ _lib = None
 
 
 def lib_path() -> str:
+    from . import build as _build
     return _build.LIB
 
 
@@ -84,6 +84,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     with _lock:
         if _lib is not None:
             return _lib
+        from . import build as _build
         path = _build.LIB
         if build_if_missing:
             path = _build.build()
