@@ -195,7 +195,7 @@ ep_status make_handle(const ep_config *cfg, void *ws, size_t ws_bytes, bool own,
     if (!out)
         return fail(EP_ERR_INVALID_ARG, "out is NULL");
     *out = nullptr;
-    Layout L;
+    Layout L{};
     ep_status st = plan(cfg, &L);
     if (st != EP_OK)
         return st;
@@ -348,7 +348,7 @@ ep_status ep_workspace_size_ex(const ep_config *cfg, size_t *bytes)
 {
     if (!bytes)
         return fail(EP_ERR_INVALID_ARG, "bytes is NULL");
-    Layout L;
+    Layout L{};
     ep_status st = plan(cfg, &L);
     if (st != EP_OK)
         return st;
