@@ -24,7 +24,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libep_gb300.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 # IEEE fp32 everywhere: no flush-to-zero, no contraction of separate adds/multiplies.
-NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2", "-ftz=false",
+NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2,-Wall,-Wextra", "-ftz=false",
               "-prec-div=true", "-prec-sqrt=true", "-fmad=false", "-I", INCLUDE, "-I", CSRC]
 
 
