@@ -44,6 +44,9 @@ namespace {
 #ifndef EP_DISPATCH_BLOCKS_PER_SM
 #define EP_DISPATCH_BLOCKS_PER_SM 64
 #endif
+#ifndef EP_DISPATCH_WIDE
+#define EP_DISPATCH_WIDE 1  // 32-byte row accesses when rows and sources are 32-byte aligned
+#endif
 #ifndef EP_COMBINE_MAX_THREADS
 #define EP_COMBINE_MAX_THREADS 256
 #endif
@@ -70,6 +73,43 @@ __device__ __forceinline__ uint4 ld_stream(const void *p)
         : "l"(p));
     return v;
 }
+
+// 32-byte vector (sm_100+ 256-bit global access): half the load/store
+// instructions of 16-byte vectors for the same bytes.
+struct alignas(32) Vec32 {
+    uint32_t w[8];
+};
+
+template <int VB>
+struct RowVec;
+
+template <>
+struct RowVec<16> {
+    using T = uint4;
+    __device__ static T load(const void *p) { return ld_stream(p); }
+    __device__ static void store(void *p, const T &v) { *static_cast<uint4 *>(p) = v; }
+};
+
+template <>
+struct RowVec<32> {
+    using T = Vec32;
+    __device__ static T load(const void *p)
+    {
+        T v;
+        asm("ld.global.nc.L1::no_allocate.v8.u32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+            : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3]), "=r"(v.w[4]), "=r"(v.w[5]),
+              "=r"(v.w[6]), "=r"(v.w[7])
+            : "l"(p));
+        return v;
+    }
+    __device__ static void store(void *p, const T &v)
+    {
+        asm volatile("st.global.v8.u32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(v.w[0]),
+                     "r"(v.w[1]), "r"(v.w[2]), "r"(v.w[3]), "r"(v.w[4]), "r"(v.w[5]), "r"(v.w[6]),
+                     "r"(v.w[7])
+                     : "memory");
+    }
+};
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
@@ -156,9 +196,15 @@ struct CombineCodec<EP_DTYPE_FP32> {
     }
 };
 
+// VB: bytes per row access of one lane (16, or 32 when every source row and
+// destination row is 32-byte aligned); a chunk is 32 lanes x kVpl accesses
+// = 4 KB either way.
+template <int VB>
 __global__ void __launch_bounds__(kDispatchThreads)
     dispatch_kernel(const __grid_constant__ DispatchArgs a)
 {
+    using RV = RowVec<VB>;
+    constexpr int kVpl = kDispatchVecPerLane * 16 / VB;
     const int lane = threadIdx.x & 31;
     const int wpb = blockDim.x >> 5;
     const long long n_slots = (long long)a.ep * a.T;
@@ -183,8 +229,8 @@ __global__ void __launch_bounds__(kDispatchThreads)
     // so the work divides finely over the resident warps even when there are
     // few slots. Every item routes its slot; the first chunk's item also
     // writes the routing state, the id plane and the scale/weight rows.
-    const int nvec = a.row_bytes >> 4;
-    const int chunk_vecs = 32 * kDispatchVecPerLane;
+    const int nvec = a.row_bytes / VB;
+    const int chunk_vecs = 32 * kVpl;
     const int nchunks = (nvec + chunk_vecs - 1) / chunk_vecs;
     const long long n_items = n_slots * nchunks;
     for (long long item = (long long)blockIdx.x * wpb + (threadIdx.x >> 5); item < n_items;
@@ -199,13 +245,13 @@ __global__ void __launch_bounds__(kDispatchThreads)
         // ---- this chunk of the hidden row, loaded before the routing so the
         // two memory round trips overlap (almost every live token is routed)
         const uint8_t *src = a.hidden[s] + (long long)t * a.row_bytes;
-        uint4 v[kDispatchVecPerLane];
+        typename RV::T v[kVpl];
         if (live) {
 #pragma unroll
-            for (int j = 0; j < kDispatchVecPerLane; ++j) {
+            for (int j = 0; j < kVpl; ++j) {
                 const int idx = c0 + j * 32 + lane;
                 if (idx < nvec)
-                    v[j] = ld_stream(src + 16 * (long long)idx);
+                    v[j] = RV::load(src + VB * (long long)idx);
             }
         }
 
@@ -272,12 +318,12 @@ __global__ void __launch_bounds__(kDispatchThreads)
         uint8_t *dst_slot = a.recv_hidden + slot * a.row_bytes;
         for (uint64_t mm = m; mm; mm &= mm - 1) {
             const int d = __ffsll((long long)mm) - 1;
-            uint4 *dst = reinterpret_cast<uint4 *>(dst_slot + d * a.hidden_stride);
+            uint8_t *dst = dst_slot + d * a.hidden_stride;
 #pragma unroll
-            for (int j = 0; j < kDispatchVecPerLane; ++j) {
+            for (int j = 0; j < kVpl; ++j) {
                 const int idx = c0 + j * 32 + lane;
                 if (idx < nvec)
-                    dst[idx] = v[j];
+                    RV::store(dst + VB * (long long)idx, v[j]);
             }
         }
         if (chunk != 0)
@@ -423,8 +469,15 @@ cudaError_t launch_dispatch(const DispatchArgs &a, cudaStream_t stream)
     const long long n_slots = (long long)a.ep * a.T;
     if (n_slots == 0 && a.eplb_bytes == 0)
         return cudaSuccess;
+    // 32-byte accesses need every source row and receive row 32-byte aligned:
+    // row_bytes % 32 == 0 (receive regions are 256-byte aligned) and every
+    // source base pointer of a rank with tokens.
+    bool wide = EP_DISPATCH_WIDE && (a.row_bytes % 32 == 0) && (a.hidden_stride % 32 == 0);
+    for (int s = 0; wide && s < a.ep; ++s)
+        if (a.num_tokens[s] > 0 && (reinterpret_cast<uintptr_t>(a.hidden[s]) % 32) != 0)
+            wide = false;
     const int wpb = kDispatchThreads / 32;
-    const int chunk_vecs = 32 * kDispatchVecPerLane;
+    const int chunk_vecs = 32 * kDispatchVecPerLane;  // 16-byte units per 4 KB chunk
     const long long n_items = n_slots * (((a.row_bytes >> 4) + chunk_vecs - 1) / chunk_vecs);
     long long blocks = (n_items + wpb - 1) / wpb;
     const long long cap = (long long)sm_count() * kDispatchBlocksPerSm;
@@ -433,7 +486,10 @@ cudaError_t launch_dispatch(const DispatchArgs &a, cudaStream_t stream)
     const long long eplb_blocks = a.eplb_bytes > 0 ? (a.ep + wpb - 1) / wpb : 0;  // one warp per rank
     if (blocks < eplb_blocks)
         blocks = eplb_blocks;
-    dispatch_kernel<<<(unsigned)blocks, kDispatchThreads, 0, stream>>>(a);
+    if (wide)
+        dispatch_kernel<32><<<(unsigned)blocks, kDispatchThreads, 0, stream>>>(a);
+    else
+        dispatch_kernel<16><<<(unsigned)blocks, kDispatchThreads, 0, stream>>>(a);
     return cudaGetLastError();
 }
 
