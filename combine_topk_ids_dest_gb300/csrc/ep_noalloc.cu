@@ -15,7 +15,9 @@
 // Host code never hands that array's name to a kernel (on the host it is a
 // stand-in, not a device address): the first call on each device, with that
 // device current, asks for the array's device address with
-// cudaGetSymbolAddress and caches it; kernels receive that pointer.
+// cudaGetSymbolAddress and caches it; kernels receive that pointer. A small
+// routing kernel fills the array from the ids; the sums are then made by the
+// library's own combine kernel, which reads the routing from it.
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -25,8 +27,6 @@
 
 namespace {
 
-constexpr int kNoallocThreads = 128;
-constexpr int kNoallocBatch = 8;
 constexpr int kMaxDevices = 64;
 
 // Routing state of up to EP_NOALLOC_MAX_SLOTS source slots (512 KB).
@@ -35,36 +35,20 @@ static __device__ __align__(256) uint64_t g_noalloc_route[EP_NOALLOC_MAX_SLOTS];
 std::mutex g_setup_mu;
 void *g_route_ptr[kMaxDevices] = {nullptr};
 
-struct NoallocArgs {
-    const int32_t *ids[epk::kMaxEp];   // source rank s: [num_tokens[s], top_k]
-    const uint16_t *eo[epk::kMaxEp];   // rank d's bf16 combine input, [ep*T, H]
-    uint16_t *out[epk::kMaxEp];        // source rank s's bf16 output, [num_tokens[s], H]
+// What the routing pass needs; the sums are computed by the library's
+// combine kernel, reading the routing bit sets from the static array.
+struct NoallocRouteArgs {
+    const int32_t *ids[epk::kMaxEp];  // source rank s: [num_tokens[s], top_k]
     int num_tokens[epk::kMaxEp];
-    uint64_t *route;                   // device address of g_noalloc_route
+    uint64_t *route;                  // device address of g_noalloc_route
     uint64_t active;
-    int ep, num_experts, experts_per_rank, top_k, T, H;
+    int ep, num_experts, experts_per_rank, top_k, T;
 };
-
-__device__ __forceinline__ uint4 ld_nc16(const void *p)
-{
-    uint4 v;
-    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-        : "l"(p));
-    return v;
-}
-
-__device__ __forceinline__ uint32_t to_bf16x2(float lo, float hi)
-{
-    uint32_t r;
-    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-    return r;
-}
 
 // One thread per slot s*T+t: the set of active ranks owning one of the
 // token's valid expert ids (0 for padding slots). Every slot of the call is
 // written, so nothing left by an earlier call is ever read.
-__global__ void noalloc_route_kernel(const __grid_constant__ NoallocArgs a)
+__global__ void noalloc_route_kernel(const __grid_constant__ NoallocRouteArgs a)
 {
     const long long n = (long long)a.ep * a.T;
     for (long long slot = (long long)blockIdx.x * blockDim.x + threadIdx.x; slot < n;
@@ -82,61 +66,6 @@ __global__ void noalloc_route_kernel(const __grid_constant__ NoallocArgs a)
             m &= a.active;
         }
         a.route[slot] = m;
-    }
-}
-
-// One thread per 16-byte column vector of one output row: ascending-rank
-// fp32 sum of the routed rows, one round to bf16.
-__global__ void __launch_bounds__(kNoallocThreads)
-    noalloc_combine_kernel(const __grid_constant__ NoallocArgs a, int blocks_per_row, long long n_blocks)
-{
-    const int nvec = a.H >> 3;
-    for (long long b = blockIdx.x; b < n_blocks; b += gridDim.x) {
-        const long long slot = b / blocks_per_row;
-        const int chunk = (int)(b - slot * blocks_per_row);
-        const int s = (int)(slot / a.T);
-        const int t = (int)(slot - (long long)s * a.T);
-        if (t >= a.num_tokens[s])
-            continue;
-        const int v = chunk * kNoallocThreads + threadIdx.x;
-        if (v >= nvec)
-            continue;
-        uint64_t mm = a.route[slot];
-        const long long off = slot * a.H * 2 + 16 * (long long)v;
-        float acc[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e)
-            acc[e] = 0.0f;
-        while (mm) {
-            uint4 x[kNoallocBatch];
-            int nb = 0;
-#pragma unroll
-            for (int j = 0; j < kNoallocBatch; ++j) {
-                if (mm) {
-                    const int d = __ffsll((long long)mm) - 1;
-                    mm &= mm - 1;
-                    x[j] = ld_nc16(reinterpret_cast<const uint8_t *>(a.eo[d]) + off);
-                    nb = j + 1;
-                }
-            }
-#pragma unroll
-            for (int j = 0; j < kNoallocBatch; ++j) {
-                if (j < nb) {
-                    const uint32_t w[4] = {x[j].x, x[j].y, x[j].z, x[j].w};
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        acc[2 * q] = __fadd_rn(acc[2 * q], __uint_as_float(w[q] << 16));
-                        acc[2 * q + 1] = __fadd_rn(acc[2 * q + 1], __uint_as_float(w[q] & 0xffff0000u));
-                    }
-                }
-            }
-        }
-        uint4 o;
-        o.x = to_bf16x2(acc[0], acc[1]);
-        o.y = to_bf16x2(acc[2], acc[3]);
-        o.z = to_bf16x2(acc[4], acc[5]);
-        o.w = to_bf16x2(acc[6], acc[7]);
-        reinterpret_cast<uint4 *>(a.out[s] + (long long)t * a.H)[v] = o;
     }
 }
 
@@ -211,19 +140,23 @@ extern "C" ep_status ep_combine_noalloc(int ep_size, int num_experts, int top_k,
         return epk::set_error(EP_ERR_INVALID_ARG, "active_rank_mask 0x%llx has bits at or above ep_size=%d",
                               (unsigned long long)mask, ep_size);
 
-    NoallocArgs a;
+    NoallocRouteArgs a;
     std::memset(&a, 0, sizeof a);
+    epk::CombineArgs c;
+    std::memset(&c, 0, sizeof c);
     for (int d = 0; d < ep_size; ++d) {
         if (!expert_output[d] || !is_aligned(expert_output[d], 16))
             return epk::set_error(EP_ERR_INVALID_ARG, "expert_output[%d] is NULL or not 16-byte aligned", d);
-        a.eo[d] = static_cast<const uint16_t *>(expert_output[d]);
+        c.eo[d] = expert_output[d];
     }
+    c.token_offset[0] = 0;
     for (int s = 0; s < ep_size; ++s) {
         const int n = num_tokens[s];
         if (n < 0 || n > tokens_per_rank)
             return epk::set_error(EP_ERR_INVALID_ARG, "num_tokens[%d]=%d outside [0, tokens_per_rank=%d]", s,
                                   n, tokens_per_rank);
-        a.num_tokens[s] = n;
+        a.num_tokens[s] = c.num_tokens[s] = n;
+        c.token_offset[s + 1] = c.token_offset[s] + n;
         if (n == 0)
             continue;
         if (!topk_ids[s] || !is_aligned(topk_ids[s], 4))
@@ -231,7 +164,7 @@ extern "C" ep_status ep_combine_noalloc(int ep_size, int num_experts, int top_k,
         if (!output[s] || !is_aligned(output[s], 16))
             return epk::set_error(EP_ERR_INVALID_ARG, "output[%d] is NULL or not 16-byte aligned", s);
         a.ids[s] = topk_ids[s];
-        a.out[s] = static_cast<uint16_t *>(output[s]);
+        c.out[s] = output[s];
     }
     uint64_t *route = nullptr;
     ep_status st = route_scratch(&route);
@@ -244,7 +177,11 @@ extern "C" ep_status ep_combine_noalloc(int ep_size, int num_experts, int top_k,
     a.experts_per_rank = num_experts / ep_size;
     a.top_k = top_k;
     a.T = tokens_per_rank;
-    a.H = hidden;
+    c.route_mask = route;
+    c.ep = ep_size;
+    c.T = tokens_per_rank;
+    c.H = hidden;
+    c.ctype = EP_DTYPE_BF16;
 
     const long long n_slots = (long long)ep_size * tokens_per_rank;
     if (n_slots == 0)
@@ -258,11 +195,7 @@ extern "C" ep_status ep_combine_noalloc(int ep_size, int num_experts, int top_k,
     cudaError_t ce = cudaGetLastError();
     if (ce != cudaSuccess)
         return epk::set_error(EP_ERR_CUDA, "ep_combine_noalloc routing launch: %s", cudaGetErrorString(ce));
-    const int bpr = (hidden / 8 + kNoallocThreads - 1) / kNoallocThreads;
-    const long long n_blocks = n_slots * bpr;
-    long long grid = n_blocks > (1LL << 30) ? (1LL << 30) : n_blocks;
-    noalloc_combine_kernel<<<(unsigned)grid, kNoallocThreads, 0, s>>>(a, bpr, n_blocks);
-    ce = cudaGetLastError();
+    ce = epk::launch_combine(c, s);  // the library's combine, reading the static routing array
     if (ce != cudaSuccess)
         return epk::set_error(EP_ERR_CUDA, "ep_combine_noalloc combine launch: %s", cudaGetErrorString(ce));
     return epk::set_error(EP_OK, "");
