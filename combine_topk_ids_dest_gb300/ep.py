@@ -46,6 +46,10 @@ class EpDispatchResult:
     eplb_global_stats: Optional[torch.Tensor] = None
 
 
+# The pages name dispatch()'s result type MoEEpDispatchResult.
+MoEEpDispatchResult = EpDispatchResult
+
+
 def _mask_value(m) -> int:
     if m is None:
         return ALL_RANKS
