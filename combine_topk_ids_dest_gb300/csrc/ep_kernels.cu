@@ -47,6 +47,9 @@ namespace {
 #ifndef EP_DISPATCH_WIDE
 #define EP_DISPATCH_WIDE 1  // 32-byte row accesses when rows and sources are 32-byte aligned
 #endif
+#ifndef EP_COMBINE_WIDE
+#define EP_COMBINE_WIDE 1  // 32-byte accesses when every row and pointer is 32-byte aligned
+#endif
 #ifndef EP_COMBINE_MAX_THREADS
 #define EP_COMBINE_MAX_THREADS 256
 #endif
@@ -352,14 +355,29 @@ __global__ void __launch_bounds__(kDispatchThreads)
     }
 }
 
-template <int CT>
+// Splits a row access of VB bytes into the 16-byte halves the codecs work on.
+__device__ __forceinline__ const uint4 &half16(const uint4 &v, int) { return v; }
+__device__ __forceinline__ uint4 half16(const Vec32 &v, int h)
+{
+    return make_uint4(v.w[4 * h], v.w[4 * h + 1], v.w[4 * h + 2], v.w[4 * h + 3]);
+}
+__device__ __forceinline__ void set_half16(uint4 &v, int, const uint4 &x) { v = x; }
+__device__ __forceinline__ void set_half16(Vec32 &v, int h, const uint4 &x)
+{
+    v.w[4 * h] = x.x, v.w[4 * h + 1] = x.y, v.w[4 * h + 2] = x.z, v.w[4 * h + 3] = x.w;
+}
+
+template <int CT, int VB>
 __global__ void __launch_bounds__(kCombineMaxThreads)
     combine_kernel(const __grid_constant__ CombineArgs a, int blocks_per_row, long long n_blocks)
 {
     using Codec = CombineCodec<CT>;
-    constexpr int kEpv = Codec::kPerVec;  // elements per 16-byte vector
+    using RV = RowVec<VB>;
+    constexpr int kEpv = Codec::kPerVec;      // elements per 16 bytes
+    constexpr int kH = VB / 16;               // 16-byte halves per access
+    constexpr int kV = kCombineVpt / kH;      // accesses per thread (same 64 bytes either way)
     const long long row_bytes = (long long)a.H * (16 / kEpv);
-    const int nvec = (int)(row_bytes >> 4);
+    const int nvec = (int)(row_bytes / VB);
     const int nthr = blockDim.x;
     for (long long b = blockIdx.x; b < n_blocks; b += gridDim.x) {
         // block -> (live token g, column chunk); g -> source rank s by binary
@@ -377,22 +395,24 @@ __global__ void __launch_bounds__(kCombineMaxThreads)
         const int s = lo;
         const int t = g - a.token_offset[s];
         const long long slot = (long long)s * a.T + t;
-        const int v0 = chunk * (nthr * kCombineVpt) + threadIdx.x;
+        const int v0 = chunk * (nthr * kV) + threadIdx.x;
         if (v0 >= nvec)
             continue;
         const uint64_t m = a.route_mask[slot];
         const long long row = slot * row_bytes;  // byte offset of the slot's row in a rank's buffer
 
-        float acc[kCombineVpt][kEpv];
+        float acc[kV][kH][kEpv];
 #pragma unroll
-        for (int j = 0; j < kCombineVpt; ++j)
+        for (int j = 0; j < kV; ++j)
 #pragma unroll
-            for (int e = 0; e < kEpv; ++e)
-                acc[j][e] = 0.0f;
+            for (int h = 0; h < kH; ++h)
+#pragma unroll
+                for (int e = 0; e < kEpv; ++e)
+                    acc[j][h][e] = 0.0f;
 
         uint64_t mm = m;
         while (mm) {
-            uint4 x[kCombineBatch][kCombineVpt];
+            typename RV::T x[kCombineBatch][kV];
             int nb = 0;
 #pragma unroll
             for (int r = 0; r < kCombineBatch; ++r) {
@@ -401,10 +421,10 @@ __global__ void __launch_bounds__(kCombineMaxThreads)
                     mm &= mm - 1;
                     const uint8_t *base = static_cast<const uint8_t *>(a.eo[d]) + row;
 #pragma unroll
-                    for (int j = 0; j < kCombineVpt; ++j) {
+                    for (int j = 0; j < kV; ++j) {
                         const int v = v0 + j * nthr;
                         if (v < nvec)
-                            x[r][j] = ld_stream(base + 16 * (long long)v);
+                            x[r][j] = RV::load(base + VB * (long long)v);
                     }
                     nb = r + 1;
                 }
@@ -413,22 +433,29 @@ __global__ void __launch_bounds__(kCombineMaxThreads)
             for (int r = 0; r < kCombineBatch; ++r) {
                 if (r < nb) {
 #pragma unroll
-                    for (int j = 0; j < kCombineVpt; ++j) {
-                        float f[kEpv];
-                        Codec::widen(x[r][j], f);
+                    for (int j = 0; j < kV; ++j)
 #pragma unroll
-                        for (int e = 0; e < kEpv; ++e)
-                            acc[j][e] = __fadd_rn(acc[j][e], f[e]);
-                    }
+                        for (int h = 0; h < kH; ++h) {
+                            float f[kEpv];
+                            Codec::widen(half16(x[r][j], h), f);
+#pragma unroll
+                            for (int e = 0; e < kEpv; ++e)
+                                acc[j][h][e] = __fadd_rn(acc[j][h][e], f[e]);
+                        }
                 }
             }
         }
-        uint4 *out = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(a.out[s]) + (long long)t * row_bytes);
+        uint8_t *out = static_cast<uint8_t *>(a.out[s]) + (long long)t * row_bytes;
 #pragma unroll
-        for (int j = 0; j < kCombineVpt; ++j) {
+        for (int j = 0; j < kV; ++j) {
             const int v = v0 + j * nthr;
-            if (v < nvec)
-                out[v] = Codec::narrow(acc[j]);
+            if (v < nvec) {
+                typename RV::T o;
+#pragma unroll
+                for (int h = 0; h < kH; ++h)
+                    set_half16(o, h, Codec::narrow(acc[j][h]));
+                RV::store(out + VB * (long long)v, o);
+            }
         }
     }
 }
@@ -506,19 +533,31 @@ cudaError_t launch_combine(const CombineArgs &a, cudaStream_t stream)
     long long grid = n_blocks;
     if (grid > (1LL << 30))
         grid = 1LL << 30;
+    // 32-byte accesses need every row of every input and output 32-byte aligned.
+    bool wide = EP_COMBINE_WIDE && (((long long)a.H * elem) % 32 == 0);
+    for (int d = 0; wide && d < a.ep; ++d)
+        if ((reinterpret_cast<uintptr_t>(a.eo[d]) % 32) != 0)
+            wide = false;
+    for (int s = 0; wide && s < a.ep; ++s)
+        if (a.num_tokens[s] > 0 && (reinterpret_cast<uintptr_t>(a.out[s]) % 32) != 0)
+            wide = false;
+#define EP_LAUNCH_COMBINE(CT)                                                                   \
+    (wide ? (combine_kernel<CT, 32><<<(unsigned)grid, threads, 0, stream>>>(a, bpr, n_blocks), 0) \
+          : (combine_kernel<CT, 16><<<(unsigned)grid, threads, 0, stream>>>(a, bpr, n_blocks), 0))
     switch (a.ctype) {
     case EP_DTYPE_BF16:
-        combine_kernel<EP_DTYPE_BF16><<<(unsigned)grid, threads, 0, stream>>>(a, bpr, n_blocks);
+        EP_LAUNCH_COMBINE(EP_DTYPE_BF16);
         break;
     case EP_DTYPE_FP16:
-        combine_kernel<EP_DTYPE_FP16><<<(unsigned)grid, threads, 0, stream>>>(a, bpr, n_blocks);
+        EP_LAUNCH_COMBINE(EP_DTYPE_FP16);
         break;
     case EP_DTYPE_FP32:
-        combine_kernel<EP_DTYPE_FP32><<<(unsigned)grid, threads, 0, stream>>>(a, bpr, n_blocks);
+        EP_LAUNCH_COMBINE(EP_DTYPE_FP32);
         break;
     default:
         return cudaErrorInvalidValue;
     }
+#undef EP_LAUNCH_COMBINE
     return cudaGetLastError();
 }
 
