@@ -534,7 +534,12 @@ cudaError_t launch_combine(const CombineArgs &a, cudaStream_t stream)
     if (grid > (1LL << 30))
         grid = 1LL << 30;
     // 32-byte accesses need every row of every input and output 32-byte aligned.
-    bool wide = EP_COMBINE_WIDE && (((long long)a.H * elem) % 32 == 0);
+    // They raise the streaming rate but also the fixed cost of a launch
+    // (measured on GB300: ~7.2 vs ~7.0 TB/s incremental, ~17 vs ~11 us fixed;
+    // equal at ~117 MB of output, faster from ~235 MB), so they are used only
+    // for large combines: output of at least 192 MiB.
+    const long long out_bytes = (long long)a.token_offset[a.ep] * a.H * elem;
+    bool wide = EP_COMBINE_WIDE && (((long long)a.H * elem) % 32 == 0) && out_bytes >= (192LL << 20);
     for (int d = 0; wide && d < a.ep; ++d)
         if ((reinterpret_cast<uintptr_t>(a.eo[d]) % 32) != 0)
             wide = false;

@@ -15,7 +15,7 @@ import torch
 
 import oracle
 import workloads
-from ep_testutil import EO_SEED, INV, bf16_bits, fill_expert_outputs, raw_bytes, to_dev
+from ep_testutil import EO_SEED, INV, fill_expert_outputs, out_bits, raw_bytes, to_dev
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
@@ -39,15 +39,27 @@ def _sample_slots(inp, rng):
     return {s: sorted(v) for s, v in picks.items()}
 
 
-@pytest.mark.parametrize("name", ["mixtral_decode", "dsv3_decode", "dsv3_prefill", "qwen3_mask"])
+# Combines whose output reaches 192 MiB take the library's 32-byte-access path;
+# these cover it for every combine type (the prefill workload covers bf16 too).
+LARGE = {
+    f"large_{cdt}": workloads.EpWorkload(
+        name=f"large_{cdt}", ep_size=4, num_experts=16, top_k=4, hidden=7168, dtype="bf16",
+        capacity=5000 if cdt == "fp32" else 9400, runtime_max=None, counts=("full",),
+        combine_dtype=cdt, dropped_ranks=(2,), seed=31)
+    for cdt in ("bf16", "fp16", "fp32")
+}
+
+
+@pytest.mark.parametrize("name", ["mixtral_decode", "dsv3_decode", "dsv3_prefill", "qwen3_mask",
+                                  "large_bf16", "large_fp16", "large_fp32"])
 def test_full_size_sampled(cuda_device, name):
     from combine_topk_ids_dest_gb300 import EpComm
-    wl = workloads.WORKLOADS[name]
+    wl = workloads.WORKLOADS[name] if name in workloads.WORKLOADS else LARGE[name]
     inp = workloads.make_inputs(wl)
     ep, E, K, H = wl.ep_size, wl.num_experts, wl.top_k, wl.hidden
     dtype = wl.torch_dtype
     comm = EpComm(ep, E, K, H, wl.capacity, dtype=dtype, enable_rank_mask=wl.enable_rank_mask,
-                  device=cuda_device)
+                  device=cuda_device, combine_dtype=wl.combine_torch_dtype)
     try:
         mask = inp.active_rank_mask if wl.enable_rank_mask else None
         res = comm.dispatch(to_dev(inp.hidden, cuda_device), to_dev(inp.topk_ids, cuda_device),
@@ -89,8 +101,10 @@ def test_full_size_sampled(cuda_device, name):
                                mask_enabled=wl.enable_rank_mask, active_rank_mask=inp.active_rank_mask,
                                row_bytes=H * wl.elem_bytes, scale_cols=wl.scale_cols)
         rows_t = torch.from_numpy(full_rows)
-        eo = [bf16_bits(workloads.expert_output_rows(EO_SEED, d, rows_t, H)) for d in range(ep)]
-        mout = oracle.combine(ep, E, K, H, Tm, m_counts, m_ids, eo, mask_enabled=wl.enable_rank_mask,
+        eo = [out_bits(workloads.expert_output_rows(EO_SEED, d, rows_t, H, dtype=wl.combine_dtype))
+              for d in range(ep)]
+        mout = oracle.combine_typed(ep, E, K, H, Tm, m_counts, m_ids, eo, wl.combine_dtype,
+                                    mask_enabled=wl.enable_rank_mask,
                               active_rank_mask=inp.active_rank_mask)
 
         live = np.array([j < m_counts[s] for s in range(ep) for j in range(Tm)])
@@ -113,7 +127,9 @@ def test_full_size_sampled(cuda_device, name):
             if not picks[s]:
                 continue
             ts = torch.tensor(picks[s], dtype=torch.long, device=cuda_device)
-            got = bf16_bits(out[s].index_select(0, ts).cpu())
+            got = out_bits(out[s].index_select(0, ts).cpu())
+            if got.dtype == np.uint32:
+                mout[s] = mout[s].view(np.uint32)
             np.testing.assert_array_equal(got, mout[s], err_msg=f"combine output of rank {s}")
     finally:
         comm.destroy()
