@@ -47,7 +47,10 @@ import workloads  # noqa: E402
 METRIC = "dispatch+combine µs/round and routed-payload GB/s as % of GB300 HBM peak"
 FALLBACK_HBM_GBS = 6800.0
 L2_FLUSH_BYTES = 256 << 20
-KERNEL_SRC = os.path.join(ROOT, "combine_topk_ids_dest_gb300", "csrc", "ep_kernels.cu")
+# Sources whose code decides what the profiled kernels do: the kernels and
+# their argument blocks.
+KERNEL_SRCS = [os.path.join(ROOT, "combine_topk_ids_dest_gb300", "csrc", f)
+               for f in ("ep_kernels.cu", "ep_internal.h")]
 
 
 # ---------------------------------------------------------------------------
@@ -99,14 +102,48 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback 6.8 TB/s (no measured peak available)"
 
 
+def _strip_comments(text: str) -> str:
+    """C/C++ source without comments and with whitespace runs collapsed, so
+    that editing a comment does not change the fingerprint of the code."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":  # string or character literal, copied whole
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
+def kernel_code_fingerprint() -> str:
+    """sha256[:16] of the kernel sources' code (comments and layout ignored)."""
+    h = hashlib.sha256()
+    for path in KERNEL_SRCS:
+        h.update(_strip_comments(open(path, encoding="utf-8").read()).encode())
+        h.update(b"\0")
+    return h.hexdigest()[:16]
+
+
 def recorded_traffic(kernel: str, workload: str):
     """DRAM bytes per launch of `kernel` from the committed ncu summary, when
-    that summary was taken on the current kernel source; else None."""
+    that summary was taken on the current kernel code; else None."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(path):
         return None
-    src = hashlib.sha256(open(KERNEL_SRC, "rb").read()).hexdigest()[:16]
-    pat = re.compile(r"^(\S+)\s+workload=(\S+)\s+dram_bytes_per_launch=(\d+)\s+source_sha256=(\S+)")
+    src = kernel_code_fingerprint()
+    pat = re.compile(r"^(\S+)\s+workload=(\S+)\s+dram_bytes_per_launch=(\d+)\s+code_sha256=(\S+)")
     for line in open(path):
         m = pat.match(line.strip())
         if m and m.group(1) == kernel and m.group(2) == workload and m.group(4) == src:

@@ -141,6 +141,8 @@ ep_status plan(const ep_config *cfg, Layout *L)
         return fail(EP_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
     if (H < 1 || ((long long)H * elem) % 16 != 0)
         return fail(EP_ERR_INVALID_ARG, "hidden=%d: a row must be a positive multiple of 16 bytes", H);
+    if ((long long)H * 4 > (1LL << 30))  // row byte counts are 32-bit in the kernels
+        return fail(EP_ERR_INVALID_ARG, "hidden=%d: rows are limited to 2^28 columns", H);
     const ep_dtype cdt = cfg->combine_dtype;
     if (cdt != EP_DTYPE_BF16 && cdt != EP_DTYPE_FP16 && cdt != EP_DTYPE_FP32)
         return fail(EP_ERR_INVALID_ARG, "combine_dtype %d: use bf16, fp16 or fp32", (int)cdt);

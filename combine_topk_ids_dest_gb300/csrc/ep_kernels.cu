@@ -3,9 +3,11 @@
 //
 // dispatch_kernel (one warp per (source slot s*T+t, column chunk of its
 // hidden row) work item, grid-stride):
-//   payload   -- the item's chunk of the hidden row is read once with 16-byte
-//                non-caching loads, issued first so they overlap the routing,
-//                and stored to every routed rank's row s*T+t.
+//   payload   -- the item's chunk of the hidden row is read once with
+//                non-caching 32-byte loads (16-byte ones when a row or source
+//                pointer is only 16-byte aligned), issued first so they
+//                overlap the routing, and stored to every routed rank's row
+//                s*T+t.
 //   routing   -- lane k reads expert id k; the owners' bits are OR-reduced
 //                across the warp (two 32-bit halves for up to 64 ranks) and
 //                ANDed with active_rank_mask (page "flashinfer.moe_ep.
@@ -18,8 +20,8 @@
 //                class description), then the scale and weight rows (one
 //                dispatch carries all four payloads).
 //
-// combine_kernel (each thread owns 4 16-byte column vectors of one live
-// token's output row):
+// combine_kernel (each thread owns 64 bytes of one live token's output row,
+// as 4 16-byte or, for large aligned combines, 2 32-byte vectors):
 //   reads the row's slot in each routed rank's combine input in ascending
 //   rank order, two ranks' loads in flight before their adds, adds in fp32
 //   from +0.0 and rounds once to bf16 (page "flashinfer.moe_ep.
@@ -27,8 +29,8 @@
 //   added up).
 //
 // Nothing here is a dense contraction; both kernels are bound by HBM
-// bandwidth, so the design is about coalesced 16-byte accesses and enough
-// bytes in flight per SM. Launch shapes come from sweeps on GB300.
+// bandwidth, so the design is about coalesced 16- and 32-byte accesses and
+// enough bytes in flight per SM. Launch shapes come from sweeps on GB300.
 #include "ep_internal.h"
 
 namespace epk {

@@ -99,7 +99,8 @@ typedef struct {
     int ep_size;               /* 1..64 ranks */
     int num_experts;           /* a positive multiple of ep_size */
     int top_k;                 /* 1..32 */
-    int hidden;                /* payload columns; hidden*elem_bytes a multiple of 16, hidden % 8 == 0 */
+    int hidden;                /* payload columns; hidden*elem_bytes a multiple of 16,
+                                  hidden % 8 == 0, hidden <= 2^28 */
     int max_tokens_per_rank;   /* capacity C >= 0 */
     ep_dtype dtype;            /* payload type of the hidden rows */
     int enable_rank_mask;      /* 0/1 */
@@ -147,8 +148,8 @@ ep_status ep_workspace_size_ex(const ep_config *cfg, size_t *bytes);
 /* Creates a handle for one EP group (MoEEpCommunication constructor with
  * MoEEpCommParams). Requirements: 1 <= ep_size <= 64; num_experts a
  * positive multiple of ep_size; 1 <= top_k <= 32; hidden > 0 with
- * hidden*elem_bytes a multiple of 16 and hidden % 8 == 0; max_tokens_per_rank
- * >= 0 with ep_size*max_tokens_per_rank <= 2^30.
+ * hidden*elem_bytes a multiple of 16, hidden % 8 == 0 and hidden <= 2^28;
+ * max_tokens_per_rank >= 0 with ep_size*max_tokens_per_rank <= 2^30.
  * enable_rank_mask (0/1) allows active_rank_mask on dispatch/combine.
  * Allocates the workspace with cudaMalloc on the current device; *out
  * receives the handle (NULL on error). */

@@ -67,12 +67,20 @@ def test_workspace_size_formula(ep_size, E, K, H, C, dt):
     ((2, 8, 2, 8, 16, 1), "16 bytes"),
     ((2, 8, 2, 256, -1, 0), "max_tokens_per_rank"),
     ((64, 64, 2, 256, (1 << 24) + 1, 0), "2^30"),
+    ((1, 8, 2, (1 << 28) + 8, 1, 0), "2^28"),
+    ((1, 8, 2, (1 << 28) + 16, 1, 1), "2^28"),
     ((2, 8, 2, 256, 16, 7), "dtype"),
 ])
 def test_workspace_size_rejects(args, frag):
     st, _ = _size(*args)
     assert st == ep.EP_ERR_INVALID_ARG
     assert frag in _lib.load().ep_last_error().decode()
+
+
+def test_workspace_size_accepts_the_widest_rows():
+    st, n = _size(1, 8, 2, 1 << 28, 1, 3)  # fp32 rows of 2^30 bytes
+    assert st == ep.EP_OK
+    assert n >= (1 << 30) + (1 << 29)  # the hidden row plus its bf16 combine row
 
 
 def test_rank_mask_helper():

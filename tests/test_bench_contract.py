@@ -71,3 +71,13 @@ def test_round_bytes_routed_pairs_match_oracle(name):
     N = inp.total_tokens
     assert b["total"] == (N * (hb + 4 * G + 4 * K + 4 * K * w) + P * (hb + 4 * G + 4 * K * w)
                           + ep * ep * T * 4 * K + P * 2 * H + 8 * N + N * 2 * H)
+
+
+def test_kernel_fingerprint_ignores_comments_only():
+    import bench
+    code = 'int f(int x) { return x /* half */ >> 1; }  // shift\nconst char *s = "a//b";\n'
+    same = '// a comment\nint f(int x)\n{\n    return x >> 1;\n}\nconst char *s = "a//b";'
+    other = 'int f(int x) { return x >> 2; }\nconst char *s = "a//b";'
+    assert bench._strip_comments(code) == bench._strip_comments(same)
+    assert bench._strip_comments(code) != bench._strip_comments(other)
+    assert '"a//b"' in bench._strip_comments(code)  # string literals are kept whole
