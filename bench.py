@@ -175,37 +175,117 @@ class _Null:
         return False
 
 
+class NvmlReader:
+    """Read-only clock, power and clock-event-reason queries on one GPU through
+    the driver's NVML library (libnvidia-ml.so.1), called with ctypes."""
+
+    # nvmlClocksEventReasons bits (public NVML API)
+    REASON_BITS = (("sw_power_cap", 0x4), ("hw_slowdown", 0x8), ("sw_thermal_slowdown", 0x20),
+                   ("hw_thermal_slowdown", 0x40), ("hw_power_brake_slowdown", 0x80))
+    CLOCK_SM = 1
+
+    def __init__(self, uuid: str):
+        import ctypes
+        self._c = ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        self.lib, self.dev = lib, ctypes.c_void_p()
+        if lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(self.dev)) != 0:
+            lib.nvmlShutdown()
+            raise RuntimeError(f"no NVML device {uuid}")
+        self._reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+
+    def _uint(self, fn, *args):
+        v = self._c.c_uint(0)
+        if fn(self.dev, *args, self._c.byref(v)) != 0:
+            raise RuntimeError(fn.__name__)
+        return v.value
+
+    def sm_mhz(self):
+        return float(self._uint(self.lib.nvmlDeviceGetClockInfo, self.CLOCK_SM))
+
+    def sm_max_mhz(self):
+        return float(self._uint(self.lib.nvmlDeviceGetMaxClockInfo, self.CLOCK_SM))
+
+    def power_w(self):
+        return self._uint(self.lib.nvmlDeviceGetPowerUsage) / 1000.0
+
+    def reasons(self):
+        v = self._c.c_ulonglong(0)
+        if self._reasons_fn(self.dev, self._c.byref(v)) != 0:
+            raise RuntimeError("clock event reasons")
+        return {name for name, bit in self.REASON_BITS if v.value & bit}
+
+    def close(self):
+        self.lib.nvmlShutdown()
+
+
 class ClockSampler:
-    """nvidia-smi clock/throttle samples every 200 ms while the timed region runs."""
+    """Samples SM clock, power and clock-event reasons while the timed region
+    runs: every 2 ms through NVML on a background thread, or, where NVML cannot
+    be loaded, every 50 ms with nvidia-smi (started, and its first sample
+    awaited, before the region begins)."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
     NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+    PERIOD_S = 0.002
 
-    def __init__(self, device):
-        self.proc, self.path = None, None
+    def __init__(self, device, reader=None):
+        self.proc, self.path, self.thread = None, None, None
+        self.samples = []  # (sm_mhz, sm_max_mhz, power_w, reasons)
         try:
             uuid = str(torch.cuda.get_device_properties(device).uuid)
-            sel = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+            self.sel = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
         except Exception:
-            sel = str(device.index or 0)
-        self.sel = sel
+            self.sel = str(device.index or 0)
+        self.reader = reader
+        if self.reader is None and self.sel.startswith("GPU-"):
+            try:
+                self.reader = NvmlReader(self.sel)
+            except Exception:
+                self.reader = None
+        self.source = "nvml" if self.reader is not None else "nvidia-smi"
+
+    def _poll(self):
+        r = self.reader
+        try:
+            smax = r.sm_max_mhz()
+            while not self._stop.is_set():
+                self.samples.append((r.sm_mhz(), smax, r.power_w(), r.reasons()))
+                self._stop.wait(self.PERIOD_S)
+        except Exception:
+            pass
 
     def __enter__(self):
+        if self.reader is not None:
+            import threading
+            self._stop = threading.Event()
+            self.thread = threading.Thread(target=self._poll, daemon=True)
+            self.thread.start()
+            return self
         try:
             fd, self.path = tempfile.mkstemp(suffix=".csv")
             self.fh = os.fdopen(fd, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", self.sel, f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=self.fh, stderr=subprocess.DEVNULL)
+            t0 = time.time()
+            while time.time() - t0 < 3 and self.proc.poll() is None and os.path.getsize(self.path) == 0:
+                time.sleep(0.01)
         except Exception:
             self.proc = None
         return self
 
     def __exit__(self, *exc):
+        if self.thread is not None:
+            self._stop.set()
+            self.thread.join(timeout=5)
+            self.reader.close()
         if self.proc is not None:
-            time.sleep(0.25)
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
@@ -214,28 +294,32 @@ class ClockSampler:
         if getattr(self, "fh", None) is not None:
             self.fh.close()
 
-    def summary(self):
-        if self.proc is None or not self.path:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        sm, smax, reasons, power = [], [], set(), []
+    def _smi_samples(self):
+        out = []
         for line in open(self.path):
             f = [x.strip() for x in line.split(",")]
             if len(f) < 9:
                 continue
             try:
-                sm.append(float(f[1]))
-                smax.append(float(f[2]))
-                power.append(float(f[3]))
+                vals = float(f[1]), float(f[2]), float(f[3])
             except ValueError:
                 continue
-            for name, v in zip(self.NAMES, f[5:9]):
-                if v.lower() == "active":
-                    reasons.add(name)
+            out.append(vals + ({n for n, v in zip(self.NAMES, f[5:9]) if v.lower() == "active"},))
         os.unlink(self.path)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
-                "samples": len(sm), "power_w_max": max(power) if power else None}
+        return out
+
+    def summary(self):
+        if self.thread is None and (self.proc is None or not self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no clock source (NVML, nvidia-smi)"]}
+        samples = self.samples if self.thread is not None else self._smi_samples()
+        if not samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "source": self.source}
+        sm = [x[0] for x in samples]
+        reasons = set().union(*(x[3] for x in samples))
+        return {"sm_mhz": statistics.median(sm), "sm_min_mhz": min(sm), "sm_max_mhz": max(x[1] for x in samples),
+                "reasons": sorted(reasons), "samples": len(samples),
+                "power_w_max": max(x[2] for x in samples), "source": self.source,
+                "period_ms": 1e3 * self.PERIOD_S if self.thread is not None else 50}
 
 
 def reduce_max(values, device=None):

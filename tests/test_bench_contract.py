@@ -81,3 +81,45 @@ def test_kernel_fingerprint_ignores_comments_only():
     assert bench._strip_comments(code) == bench._strip_comments(same)
     assert bench._strip_comments(code) != bench._strip_comments(other)
     assert '"a//b"' in bench._strip_comments(code)  # string literals are kept whole
+
+
+class _FakeNvml:
+    """Stands in for the NVML reader: a clock that drops once, a power-cap reason."""
+
+    def __init__(self):
+        self.n, self.closed = 0, False
+
+    def sm_max_mhz(self):
+        return 2070.0
+
+    def sm_mhz(self):
+        self.n += 1
+        return 1900.0 if self.n == 3 else 2070.0
+
+    def power_w(self):
+        return 600.0 + self.n
+
+    def reasons(self):
+        return {"sw_power_cap"} if self.n == 3 else set()
+
+    def close(self):
+        self.closed = True
+
+
+def test_clock_sampler_summarises_reader_samples():
+    import time
+
+    import torch
+
+    import bench
+    fake = _FakeNvml()
+    cs = bench.ClockSampler(torch.device("cpu"), reader=fake)
+    with cs:
+        t0 = time.time()
+        while fake.n < 5 and time.time() - t0 < 10:
+            time.sleep(0.005)
+    s = cs.summary()
+    assert fake.closed and s["source"] == "nvml"
+    assert s["samples"] >= 5 and s["sm_mhz"] == 2070.0 and s["sm_min_mhz"] == 1900.0
+    assert s["sm_max_mhz"] == 2070.0 and s["reasons"] == ["sw_power_cap"]
+    assert s["power_w_max"] >= 605.0
