@@ -40,6 +40,80 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
+class NvmlReader:
+    """Read-only clock, power and clock-event-reason queries on one GPU through
+    the driver's NVML library (libnvidia-ml.so.1), called with ctypes."""
+
+    # nvmlClocksEventReasons bits (public NVML API)
+    REASON_BITS = (("sw_power_cap", 0x4), ("hw_slowdown", 0x8), ("sw_thermal_slowdown", 0x20),
+                   ("hw_thermal_slowdown", 0x40), ("hw_power_brake_slowdown", 0x80))
+    CLOCK_SM = 1
+
+    def __init__(self, uuid: str):
+        import ctypes
+        self._c = ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        self.lib, self.dev = lib, ctypes.c_void_p()
+        if lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(self.dev)) != 0:
+            lib.nvmlShutdown()
+            raise RuntimeError(f"no NVML device {uuid}")
+        self._reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+
+    def _uint(self, fn, *args):
+        v = self._c.c_uint(0)
+        if fn(self.dev, *args, self._c.byref(v)) != 0:
+            raise RuntimeError(fn.__name__)
+        return v.value
+
+    def sm_mhz(self):
+        return float(self._uint(self.lib.nvmlDeviceGetClockInfo, self.CLOCK_SM))
+
+    def sm_max_mhz(self):
+        return float(self._uint(self.lib.nvmlDeviceGetMaxClockInfo, self.CLOCK_SM))
+
+    def power_w(self):
+        return self._uint(self.lib.nvmlDeviceGetPowerUsage) / 1000.0
+
+    def reason_bits(self):
+        v = self._c.c_ulonglong(0)
+        if self._reasons_fn(self.dev, self._c.byref(v)) != 0:
+            raise RuntimeError("clock event reasons")
+        return v.value
+
+    def close(self):
+        self.lib.nvmlShutdown()
+
+
+def clock_poller(reader, period_s: float, out, stop) -> int:
+    """Writes "ready" once, then one line "sm_mhz,sm_max_mhz,power_w,reason_bits"
+    every period_s until stop() is true. Runs in its own process (below), so
+    it never competes with the timed launches for the interpreter lock."""
+    smax = reader.sm_max_mhz()
+    out.write("ready\n")
+    out.flush()
+    while not stop():
+        out.write(f"{reader.sm_mhz()},{smax},{reader.power_w()},{reader.reason_bits()}\n")
+        time.sleep(period_s)
+    out.flush()
+    reader.close()
+    return 0
+
+
+if __name__ == "__main__" and sys.argv[1:2] == ["--clock-poller"]:
+    import signal
+    _stop = []
+    signal.signal(signal.SIGTERM, lambda *_: _stop.append(1))
+    try:
+        _reader = NvmlReader(sys.argv[2])
+    except Exception as e:  # no NVML here: the parent falls back to nvidia-smi
+        print(f"unavailable: {e}", flush=True)
+        sys.exit(0)
+    sys.exit(clock_poller(_reader, float(sys.argv[3]), sys.stdout, lambda: bool(_stop)))
+
+
 import torch  # noqa: E402
 
 import workloads  # noqa: E402
@@ -175,128 +249,88 @@ class _Null:
         return False
 
 
-class NvmlReader:
-    """Read-only clock, power and clock-event-reason queries on one GPU through
-    the driver's NVML library (libnvidia-ml.so.1), called with ctypes."""
-
-    # nvmlClocksEventReasons bits (public NVML API)
-    REASON_BITS = (("sw_power_cap", 0x4), ("hw_slowdown", 0x8), ("sw_thermal_slowdown", 0x20),
-                   ("hw_thermal_slowdown", 0x40), ("hw_power_brake_slowdown", 0x80))
-    CLOCK_SM = 1
-
-    def __init__(self, uuid: str):
-        import ctypes
-        self._c = ctypes
-        lib = ctypes.CDLL("libnvidia-ml.so.1")
-        if lib.nvmlInit_v2() != 0:
-            raise RuntimeError("nvmlInit failed")
-        self.lib, self.dev = lib, ctypes.c_void_p()
-        if lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(self.dev)) != 0:
-            lib.nvmlShutdown()
-            raise RuntimeError(f"no NVML device {uuid}")
-        self._reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
-            lib.nvmlDeviceGetCurrentClocksThrottleReasons
-
-    def _uint(self, fn, *args):
-        v = self._c.c_uint(0)
-        if fn(self.dev, *args, self._c.byref(v)) != 0:
-            raise RuntimeError(fn.__name__)
-        return v.value
-
-    def sm_mhz(self):
-        return float(self._uint(self.lib.nvmlDeviceGetClockInfo, self.CLOCK_SM))
-
-    def sm_max_mhz(self):
-        return float(self._uint(self.lib.nvmlDeviceGetMaxClockInfo, self.CLOCK_SM))
-
-    def power_w(self):
-        return self._uint(self.lib.nvmlDeviceGetPowerUsage) / 1000.0
-
-    def reasons(self):
-        v = self._c.c_ulonglong(0)
-        if self._reasons_fn(self.dev, self._c.byref(v)) != 0:
-            raise RuntimeError("clock event reasons")
-        return {name for name, bit in self.REASON_BITS if v.value & bit}
-
-    def close(self):
-        self.lib.nvmlShutdown()
-
-
 class ClockSampler:
     """Samples SM clock, power and clock-event reasons while the timed region
-    runs: every 2 ms through NVML on a background thread, or, where NVML cannot
-    be loaded, every 50 ms with nvidia-smi (started, and its first sample
-    awaited, before the region begins)."""
+    runs: every 2 ms through NVML in a separate process (this file run with
+    --clock-poller), or, where NVML cannot be loaded, every 50 ms with
+    nvidia-smi. Either sampler is started, and its first line awaited, before
+    the region begins."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
     NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
-    PERIOD_S = 0.002
+    NVML_PERIOD_S = 0.002
+    SMI_PERIOD_MS = 50
 
-    def __init__(self, device, reader=None):
-        self.proc, self.path, self.thread = None, None, None
-        self.samples = []  # (sm_mhz, sm_max_mhz, power_w, reasons)
+    def __init__(self, device):
+        self.proc, self.path, self.source = None, None, None
         try:
             uuid = str(torch.cuda.get_device_properties(device).uuid)
             self.sel = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
         except Exception:
             self.sel = str(device.index or 0)
-        self.reader = reader
-        if self.reader is None and self.sel.startswith("GPU-"):
-            try:
-                self.reader = NvmlReader(self.sel)
-            except Exception:
-                self.reader = None
-        self.source = "nvml" if self.reader is not None else "nvidia-smi"
 
-    def _poll(self):
-        r = self.reader
-        try:
-            smax = r.sm_max_mhz()
-            while not self._stop.is_set():
-                self.samples.append((r.sm_mhz(), smax, r.power_w(), r.reasons()))
-                self._stop.wait(self.PERIOD_S)
-        except Exception:
-            pass
+    def _start(self, cmd):
+        if self.path:
+            os.unlink(self.path)
+        fd, self.path = tempfile.mkstemp(suffix=".clk")
+        with os.fdopen(fd, "w") as fh:
+            self.proc = subprocess.Popen(cmd, stdout=fh, stderr=subprocess.DEVNULL, stdin=subprocess.DEVNULL)
+        t0 = time.time()
+        while time.time() - t0 < 20 and self.proc.poll() is None and os.path.getsize(self.path) == 0:
+            time.sleep(0.005)
+        with open(self.path) as f:
+            first = f.readline()
+        return first
 
     def __enter__(self):
-        if self.reader is not None:
-            import threading
-            self._stop = threading.Event()
-            self.thread = threading.Thread(target=self._poll, daemon=True)
-            self.thread.start()
-            return self
         try:
-            fd, self.path = tempfile.mkstemp(suffix=".csv")
-            self.fh = os.fdopen(fd, "w")
-            self.proc = subprocess.Popen(["nvidia-smi", "-i", self.sel, f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "50"],
-                                         stdout=self.fh, stderr=subprocess.DEVNULL)
-            t0 = time.time()
-            while time.time() - t0 < 3 and self.proc.poll() is None and os.path.getsize(self.path) == 0:
-                time.sleep(0.01)
+            if self.sel.startswith("GPU-"):
+                first = self._start([sys.executable, os.path.abspath(__file__), "--clock-poller", self.sel,
+                                     str(self.NVML_PERIOD_S)])
+                if first.startswith("ready"):
+                    self.source = "nvml"
+                    return self
+                self._stop()
+            self._start(["nvidia-smi", "-i", self.sel, f"--query-gpu={self.FIELDS}",
+                         "--format=csv,noheader,nounits", "-lms", str(self.SMI_PERIOD_MS)])
+            self.source = "nvidia-smi"
         except Exception:
-            self.proc = None
+            self._stop()
         return self
 
-    def __exit__(self, *exc):
-        if self.thread is not None:
-            self._stop.set()
-            self.thread.join(timeout=5)
-            self.reader.close()
+    def _stop(self):
         if self.proc is not None:
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
             except Exception:
                 self.proc.kill()
-        if getattr(self, "fh", None) is not None:
-            self.fh.close()
+                self.proc.wait()
+            self.proc = None
 
-    def _smi_samples(self):
+    def __exit__(self, *exc):
+        self._stop()
+
+    @staticmethod
+    def parse_nvml(lines):
         out = []
-        for line in open(self.path):
+        for line in lines:
+            f = line.strip().split(",")
+            if len(f) != 4:
+                continue
+            try:
+                sm, smax, pw, bits = float(f[0]), float(f[1]), float(f[2]), int(f[3])
+            except ValueError:
+                continue
+            out.append((sm, smax, pw, {n for n, b in NvmlReader.REASON_BITS if bits & b}))
+        return out
+
+    @classmethod
+    def parse_smi(cls, lines):
+        out = []
+        for line in lines:
             f = [x.strip() for x in line.split(",")]
             if len(f) < 9:
                 continue
@@ -304,22 +338,28 @@ class ClockSampler:
                 vals = float(f[1]), float(f[2]), float(f[3])
             except ValueError:
                 continue
-            out.append(vals + ({n for n, v in zip(self.NAMES, f[5:9]) if v.lower() == "active"},))
-        os.unlink(self.path)
+            out.append(vals + ({n for n, v in zip(cls.NAMES, f[5:9]) if v.lower() == "active"},))
         return out
 
-    def summary(self):
-        if self.thread is None and (self.proc is None or not self.path):
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no clock source (NVML, nvidia-smi)"]}
-        samples = self.samples if self.thread is not None else self._smi_samples()
+    @staticmethod
+    def summarise(samples, source, period_ms):
         if not samples:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "source": self.source}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "source": source}
         sm = [x[0] for x in samples]
-        reasons = set().union(*(x[3] for x in samples))
-        return {"sm_mhz": statistics.median(sm), "sm_min_mhz": min(sm), "sm_max_mhz": max(x[1] for x in samples),
-                "reasons": sorted(reasons), "samples": len(samples),
-                "power_w_max": max(x[2] for x in samples), "source": self.source,
-                "period_ms": 1e3 * self.PERIOD_S if self.thread is not None else 50}
+        return {"sm_mhz": statistics.median(sm), "sm_min_mhz": min(sm),
+                "sm_max_mhz": max(x[1] for x in samples),
+                "reasons": sorted(set().union(*(x[3] for x in samples))), "samples": len(samples),
+                "power_w_max": max(x[2] for x in samples), "source": source, "period_ms": period_ms}
+
+    def summary(self):
+        if self.source is None or not self.path:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no clock source (NVML, nvidia-smi)"]}
+        with open(self.path) as f:
+            lines = f.readlines()
+        os.unlink(self.path)
+        if self.source == "nvml":
+            return self.summarise(self.parse_nvml(lines), "nvml", 1e3 * self.NVML_PERIOD_S)
+        return self.summarise(self.parse_smi(lines), "nvidia-smi", self.SMI_PERIOD_MS)
 
 
 def reduce_max(values, device=None):

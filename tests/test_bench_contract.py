@@ -99,27 +99,38 @@ class _FakeNvml:
     def power_w(self):
         return 600.0 + self.n
 
-    def reasons(self):
-        return {"sw_power_cap"} if self.n == 3 else set()
+    def reason_bits(self):
+        return 0x4 if self.n == 3 else 0  # sw_power_cap
 
     def close(self):
         self.closed = True
 
 
-def test_clock_sampler_summarises_reader_samples():
-    import time
-
-    import torch
+def test_clock_poller_lines_and_summary():
+    import io
 
     import bench
-    fake = _FakeNvml()
-    cs = bench.ClockSampler(torch.device("cpu"), reader=fake)
-    with cs:
-        t0 = time.time()
-        while fake.n < 5 and time.time() - t0 < 10:
-            time.sleep(0.005)
-    s = cs.summary()
-    assert fake.closed and s["source"] == "nvml"
-    assert s["samples"] >= 5 and s["sm_mhz"] == 2070.0 and s["sm_min_mhz"] == 1900.0
-    assert s["sm_max_mhz"] == 2070.0 and s["reasons"] == ["sw_power_cap"]
-    assert s["power_w_max"] >= 605.0
+    fake, out = _FakeNvml(), io.StringIO()
+    assert bench.clock_poller(fake, 0.0, out, lambda: fake.n >= 5) == 0
+    lines = out.getvalue().splitlines()
+    assert lines[0] == "ready" and len(lines) == 6 and fake.closed
+    s = bench.ClockSampler.summarise(bench.ClockSampler.parse_nvml(lines[1:]), "nvml", 2.0)
+    assert s["samples"] == 5 and s["sm_mhz"] == 2070.0 and s["sm_min_mhz"] == 1900.0
+    assert s["sm_max_mhz"] == 2070.0 and s["reasons"] == ["sw_power_cap"] and s["power_w_max"] == 605.0
+
+
+def test_clock_smi_lines_parse():
+    import bench
+    lines = ["0, 2070, 2070, 650.5, 0x0000000000000004, Not Active, Not Active, Not Active, Active",
+             "0, 1995, 2070, 700.0, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active",
+             "garbage"]
+    s = bench.ClockSampler.summarise(bench.ClockSampler.parse_smi(lines), "nvidia-smi", 50)
+    assert s["samples"] == 2 and s["sm_min_mhz"] == 1995.0 and s["reasons"] == ["sw_power_cap"]
+
+
+def test_clock_poller_process_reports_unavailable_without_nvml():
+    # No GPU has this UUID (and here there is no NVML at all): the poller process
+    # says so and exits 0, and the sampler then falls back to nvidia-smi.
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--clock-poller", "GPU-none", "0.002"],
+                       capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0 and r.stdout.startswith("unavailable")
