@@ -1,6 +1,9 @@
 """ctypes declarations of the C ABI in include/ep.h (libep_gb300.so).
 
 Loading fails loudly: there is no fallback implementation of any operation.
+With EP_GB300_CHECKED=1 in the environment the checked build
+(libep_gb300_checked.so: every kernel access tested against its buffer,
+EP_ERR_DEVICE_CHECK on a violation) is loaded instead.
 """
 from __future__ import annotations
 
@@ -15,8 +18,14 @@ EP_ERR_STATE = 2
 EP_ERR_CUDA = 3
 EP_ERR_OOM = 4
 EP_ERR_UNSUPPORTED = 5
+EP_ERR_DEVICE_CHECK = 6
 STATUS_NAMES = {0: "EP_OK", 1: "EP_ERR_INVALID_ARG", 2: "EP_ERR_STATE", 3: "EP_ERR_CUDA",
-                4: "EP_ERR_OOM", 5: "EP_ERR_UNSUPPORTED"}
+                4: "EP_ERR_OOM", 5: "EP_ERR_UNSUPPORTED", 6: "EP_ERR_DEVICE_CHECK"}
+
+# Access sites of the checked build (enum CheckSite in csrc/ep_internal.h).
+CHECK_SITES = ("src_hidden", "src_ids", "src_scale", "src_weights", "recv_hidden", "recv_ids",
+               "recv_scale", "recv_weights", "route_write", "eplb_src", "eplb_dst", "route_read",
+               "combine_in", "combine_out", "noalloc_ids", "noalloc_route")
 
 EP_DTYPE_BF16 = 0
 EP_DTYPE_FP8_E4M3 = 1
@@ -73,21 +82,27 @@ _lock = threading.Lock()
 _lib = None
 
 
+def checked() -> bool:
+    """True when this process uses the checked build (EP_GB300_CHECKED=1)."""
+    return os.environ.get("EP_GB300_CHECKED", "0") == "1"
+
+
 def lib_path() -> str:
     from . import build as _build
-    return _build.LIB
+    return _build.LIB_CHECKED if checked() else _build.LIB
 
 
 def load(build_if_missing: bool = True) -> ctypes.CDLL:
-    """Load libep_gb300.so (building it first if it is missing or stale)."""
+    """Load libep_gb300.so, or libep_gb300_checked.so under EP_GB300_CHECKED=1
+    (building it first if it is missing or stale)."""
     global _lib
     with _lock:
         if _lib is not None:
             return _lib
         from . import build as _build
-        path = _build.LIB
+        path = lib_path()
         if build_if_missing:
-            path = _build.build()
+            path = _build.build(checked=checked())
         if not os.path.exists(path):
             raise ImportError(f"CUDA library {path} is missing; run "
                               "`python -m combine_topk_ids_dest_gb300.build`")
@@ -123,6 +138,9 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         L.ep_combine_noalloc.restype = i32
         L.ep_last_error.argtypes = []
         L.ep_last_error.restype = ctypes.c_char_p
+        if checked():
+            L.ep_checked_trim_extent.argtypes = [i32, ctypes.c_longlong]
+            L.ep_checked_trim_extent.restype = i32
         _lib = L
         return L
 

@@ -29,6 +29,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 #include <new>
 
 #include <nvtx3/nvToolsExt.h>
@@ -209,6 +210,11 @@ ep_status make_handle(const ep_config *cfg, void *ws, size_t ws_bytes, bool own,
         return fail(EP_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(ce));
     if (!ep_is_supported())
         return fail(EP_ERR_UNSUPPORTED, "device %d is not compute capability 10.3 (sm_103)", dev);
+#if EP_CHECKED
+    // look the check record up now, outside any stream capture a later call may be in
+    if (!epk::check_record())
+        return EP_ERR_CUDA;
+#endif
     if (own) {
         void *p = nullptr;
         ce = cudaMalloc(&p, L.total);
@@ -320,6 +326,104 @@ ep_status epk::set_error(ep_status st, const char *fmt, ...)
     va_end(ap);
     return st;
 }
+
+const char *epk::check_site_name(int site)
+{
+    static const char *const names[kNumSites] = {
+        "dispatch: source hidden row", "dispatch: source id row", "dispatch: source scale row",
+        "dispatch: source weight row", "dispatch: receive hidden row", "dispatch: receive id row",
+        "dispatch: receive scale row", "dispatch: receive weight row", "dispatch: routing state",
+        "dispatch: eplb_local_stats", "dispatch: gathered eplb stats", "combine: routing state",
+        "combine: expert output row", "combine: output row", "ep_combine_noalloc: id row",
+        "ep_combine_noalloc: routing scratch"};
+    return (site >= 0 && site < kNumSites) ? names[site] : "unknown site";
+}
+
+#if EP_CHECKED
+namespace {
+
+// One check record per device for the whole library: {violations, first
+// site, first offset, that buffer's extent}.
+__device__ unsigned long long g_check_rec[4];
+
+std::mutex g_check_mu;
+void *g_check_ptr[64] = {nullptr};
+int g_trim_site = -1;
+long long g_trim_bytes = 0;
+
+}  // namespace
+
+unsigned long long *epk::check_record()
+{
+    int dev = -1;
+    cudaError_t ce = cudaGetDevice(&dev);
+    if (ce != cudaSuccess || dev < 0 || dev >= 64) {
+        set_error(EP_ERR_CUDA, "check record: no usable current device");
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lock(g_check_mu);
+    if (!g_check_ptr[dev]) {
+        void *p = nullptr;
+        ce = cudaGetSymbolAddress(&p, g_check_rec);
+        if (ce != cudaSuccess || !p) {
+            cudaGetLastError();
+            set_error(EP_ERR_CUDA, "cudaGetSymbolAddress of the check record: %s", cudaGetErrorString(ce));
+            return nullptr;
+        }
+        g_check_ptr[dev] = p;
+    }
+    return static_cast<unsigned long long *>(g_check_ptr[dev]);
+}
+
+epk::CheckCtx epk::check_ctx(unsigned long long *rec)
+{
+    std::lock_guard<std::mutex> lock(g_check_mu);
+    return CheckCtx{rec, g_trim_site, g_trim_bytes};
+}
+
+ep_status epk::check_after(unsigned long long *rec, cudaStream_t stream, const char *what)
+{
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaError_t ce = cudaStreamIsCapturing(stream, &cs);
+    if (ce != cudaSuccess)
+        return set_error(EP_ERR_CUDA, "%s: cudaStreamIsCapturing: %s", what, cudaGetErrorString(ce));
+    if (cs != cudaStreamCaptureStatusNone)
+        return EP_OK;  // checked at the next call outside the capture
+    ce = cudaStreamSynchronize(stream);
+    unsigned long long h[4] = {0, 0, 0, 0};
+    if (ce == cudaSuccess)
+        ce = cudaMemcpy(h, rec, sizeof h, cudaMemcpyDeviceToHost);
+    if (ce != cudaSuccess)
+        return set_error(EP_ERR_CUDA, "%s: reading the check record: %s", what, cudaGetErrorString(ce));
+    if (h[0] == 0)
+        return EP_OK;
+    cudaMemset(rec, 0, sizeof h);
+    return set_error(EP_ERR_DEVICE_CHECK,
+                     "%s: %llu device accesses fell outside their buffers and were skipped; the first: %s, "
+                     "byte offset %lld of a %lld-byte buffer",
+                     what, h[0], check_site_name((int)h[1]), (long long)h[2], (long long)h[3]);
+}
+
+// Test hook of the checked build (not part of include/ep.h): declares every
+// buffer of one access site `bytes` shorter than it is, so that accesses
+// near its end, which stay inside the real buffer, are reported and
+// skipped. site = -1 clears it.
+extern "C" __attribute__((visibility("default"))) ep_status ep_checked_trim_extent(int site, long long bytes)
+{
+    if (site < -1 || site >= epk::kNumSites || bytes < 0)
+        return epk::set_error(EP_ERR_INVALID_ARG, "site %d / bytes %lld", site, bytes);
+    std::lock_guard<std::mutex> lock(g_check_mu);
+    g_trim_site = site;
+    g_trim_bytes = site < 0 ? 0 : bytes;
+    return epk::set_error(EP_OK, "");
+}
+#else
+unsigned long long *epk::check_record() { return nullptr; }
+
+epk::CheckCtx epk::check_ctx(unsigned long long *) { return CheckCtx{nullptr, -1, 0}; }
+
+ep_status epk::check_after(unsigned long long *, cudaStream_t, const char *) { return EP_OK; }
+#endif
 
 extern "C" {
 
@@ -488,6 +592,13 @@ ep_status ep_dispatch_ex(ep_handle *h, const ep_dispatch_args *args, void *strea
     a.has_weights = topk_weights ? 1 : 0;
     a.eplb_dst = h->ws + h->off_eplb;
     a.eplb_bytes = eplb_bytes;
+    unsigned long long *rec = nullptr;
+#if EP_CHECKED
+    rec = epk::check_record();
+    if (!rec)
+        return EP_ERR_CUDA;
+#endif
+    a.chk = epk::check_ctx(rec);
 
     nvtxRangePushA("ep_dispatch");  // host-side range around the launch, for profilers
     cudaError_t ce = epk::launch_dispatch(a, static_cast<cudaStream_t>(stream));
@@ -510,7 +621,8 @@ ep_status ep_dispatch_ex(ep_handle *h, const ep_dispatch_args *args, void *strea
         out->eplb_global_stats = eplb_bytes ? h->ws + h->off_eplb : nullptr;
         out->eplb_stats_bytes = eplb_bytes;
     }
-    return ok();
+    st = epk::check_after(rec, static_cast<cudaStream_t>(stream), "ep_dispatch");
+    return st == EP_OK ? ok() : st;
 }
 
 ep_status ep_get_combine_input_buffer(ep_handle *h, int rank, void **out)
@@ -571,6 +683,13 @@ ep_status ep_combine(ep_handle *h, const void *const *expert_output, void *const
     a.T = h->T;
     a.H = h->hidden;
     a.ctype = (int)h->combine_dtype;
+    unsigned long long *rec = nullptr;
+#if EP_CHECKED
+    rec = epk::check_record();
+    if (!rec)
+        return EP_ERR_CUDA;
+#endif
+    a.chk = epk::check_ctx(rec);
 
     nvtxRangePushA("ep_combine");
     cudaError_t ce = epk::launch_combine(a, static_cast<cudaStream_t>(stream));
@@ -578,7 +697,8 @@ ep_status ep_combine(ep_handle *h, const void *const *expert_output, void *const
     if (ce != cudaSuccess)
         return fail(EP_ERR_CUDA, "combine launch: %s", cudaGetErrorString(ce));
     h->pending = false;
-    return ok();
+    st = epk::check_after(rec, static_cast<cudaStream_t>(stream), "ep_combine");
+    return st == EP_OK ? ok() : st;
 }
 
 ep_status ep_destroy(ep_handle *h)

@@ -10,9 +10,64 @@
 
 #include "ep.h"
 
+#ifndef EP_CHECKED
+#define EP_CHECKED 0
+#endif
+
 namespace epk {
 
 constexpr int kMaxEp = EP_MAX_EP_SIZE;
+
+// Checked build (EP_CHECKED=1, libep_gb300_checked.so): every global access
+// of the kernels is tested against the extent of the buffer it belongs to
+// (the extents the C ABI documents); an access outside is skipped and
+// recorded, and the host turns the record into EP_ERR_DEVICE_CHECK. In the
+// normal build the tests compile to nothing. Access sites, for the record:
+enum CheckSite {
+    kSiteSrcHidden = 0, kSiteSrcIds, kSiteSrcScale, kSiteSrcWeights,
+    kSiteRecvHidden, kSiteRecvIds, kSiteRecvScale, kSiteRecvWeights,
+    kSiteRouteWrite, kSiteEplbSrc, kSiteEplbDst,
+    kSiteRouteRead, kSiteCombineIn, kSiteCombineOut,
+    kSiteNoallocIds, kSiteNoallocRoute,
+    kNumSites
+};
+
+// What a checked launch needs: the device record {violations, first site,
+// first offset (signed, bytes from the buffer's start), that buffer's
+// extent in bytes}, and a test hook that declares one site's buffers
+// `trim_bytes` shorter than they are.
+struct CheckCtx {
+    unsigned long long *rec;  // 4 entries, device; NULL in the normal build
+    int trim_site;            // -1: none
+    long long trim_bytes;
+};
+
+// Name of a check site, for messages.
+const char *check_site_name(int site);
+
+#if EP_CHECKED && defined(__CUDACC__)
+// True when [p, p + nb) lies inside [lo, lo + extent) (the extent shortened
+// by the test hook's trim at its site); otherwise records the access and
+// returns false, so the caller skips it.
+static __device__ __noinline__ bool in_bounds(const CheckCtx &c, int site, const void *p, int nb,
+                                          const void *lo, long long extent)
+{
+    if (site == c.trim_site)
+        extent -= c.trim_bytes;
+    const long long off = static_cast<const char *>(p) - static_cast<const char *>(lo);
+    if (off >= 0 && off + nb <= extent)
+        return true;
+    if (atomicAdd(&c.rec[0], 1ULL) == 0ULL) {
+        c.rec[1] = static_cast<unsigned long long>(site);
+        c.rec[2] = static_cast<unsigned long long>(off);
+        c.rec[3] = static_cast<unsigned long long>(extent);
+    }
+    return false;
+}
+#define EP_IN_BOUNDS(ctx, site, p, nb, lo, extent) ::epk::in_bounds((ctx), (site), (p), (nb), (lo), (extent))
+#else
+#define EP_IN_BOUNDS(ctx, site, p, nb, lo, extent) true
+#endif
 
 // Everything one dispatch launch needs, passed by value as a __grid_constant__
 // kernel parameter (about 2.4 KB), so no host->device copy precedes a launch
@@ -47,6 +102,8 @@ struct DispatchArgs {
     const uint8_t *eplb_src[kMaxEp];
     uint8_t *eplb_dst;
     int eplb_bytes;  // 0 = nothing to gather; else a multiple of 4
+
+    CheckCtx chk;
 };
 
 struct CombineArgs {
@@ -58,6 +115,8 @@ struct CombineArgs {
     const uint64_t *route_mask;    // [ep*T], written by the dispatch
     int ep, T, H;
     int ctype;  // element type of eo/out: EP_DTYPE_BF16, EP_DTYPE_FP16 or EP_DTYPE_FP32
+
+    CheckCtx chk;
 };
 
 // Records `fmt` as the calling thread's ep_last_error() message (cleared for
@@ -67,5 +126,19 @@ ep_status set_error(ep_status st, const char *fmt, ...);
 // Queue one launch on `stream`; returns the launch's cudaError_t.
 cudaError_t launch_dispatch(const DispatchArgs &a, cudaStream_t stream);
 cudaError_t launch_combine(const CombineArgs &a, cudaStream_t stream);
+
+// Checked build: the CheckCtx for a launch recording into `rec`, with the
+// test hook's trim applied; and, after the launch, EP_OK or
+// EP_ERR_DEVICE_CHECK from the record (which is then cleared). `what` names
+// the call for the message. Outside stream capture it synchronizes
+// `stream`; during a capture it returns EP_OK and leaves the record for the
+// next check. The normal build returns {NULL, -1, 0} and EP_OK.
+CheckCtx check_ctx(unsigned long long *rec);
+ep_status check_after(unsigned long long *rec, cudaStream_t stream, const char *what);
+
+// Checked build: device address of the library's check record on the
+// current device (one static record per device, shared by every handle and
+// call); NULL on failure (ep_last_error set). The normal build returns NULL.
+unsigned long long *check_record();
 
 }  // namespace epk

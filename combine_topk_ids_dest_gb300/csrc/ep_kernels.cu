@@ -224,8 +224,13 @@ __global__ void __launch_bounds__(kDispatchThreads)
             const int r = (int)gw;
             const uint32_t *src = reinterpret_cast<const uint32_t *>(a.eplb_src[r]);
             uint32_t *dst = reinterpret_cast<uint32_t *>(a.eplb_dst + (long long)r * a.eplb_bytes);
-            for (int w = lane; w < (a.eplb_bytes >> 2); w += 32)
-                dst[w] = src[w];
+            for (int w = lane; w < (a.eplb_bytes >> 2); w += 32) {
+                uint32_t x = 0;
+                if (EP_IN_BOUNDS(a.chk, kSiteEplbSrc, src + w, 4, a.eplb_src[r], a.eplb_bytes))
+                    x = src[w];
+                if (EP_IN_BOUNDS(a.chk, kSiteEplbDst, dst + w, 4, a.eplb_dst, (long long)a.ep * a.eplb_bytes))
+                    dst[w] = x;
+            }
         }
     }
 
@@ -251,11 +256,17 @@ __global__ void __launch_bounds__(kDispatchThreads)
         // two memory round trips overlap (almost every live token is routed)
         const uint8_t *src = a.hidden[s] + (long long)t * a.row_bytes;
         typename RV::T v[kVpl];
+#if EP_CHECKED
+#pragma unroll
+        for (int j = 0; j < kVpl; ++j)
+            v[j] = typename RV::T{};
+#endif
         if (live) {
 #pragma unroll
             for (int j = 0; j < kVpl; ++j) {
                 const int idx = c0 + j * 32 + lane;
-                if (idx < nvec)
+                if (idx < nvec && EP_IN_BOUNDS(a.chk, kSiteSrcHidden, src + VB * (long long)idx, VB, a.hidden[s],
+                                               (long long)a.num_tokens[s] * a.row_bytes))
                     v[j] = RV::load(src + VB * (long long)idx);
             }
         }
@@ -264,7 +275,9 @@ __global__ void __launch_bounds__(kDispatchThreads)
         int my_id = EP_INVALID_EXPERT_ID;
         unsigned lo = 0, hi = 0;
         if (live && lane < K) {
-            my_id = a.ids[s][(long long)t * K + lane];
+            const int32_t *ip = a.ids[s] + (long long)t * K + lane;
+            if (EP_IN_BOUNDS(a.chk, kSiteSrcIds, ip, 4, a.ids[s], (long long)a.num_tokens[s] * K * 4))
+                my_id = *ip;
             if (my_id >= 0 && my_id < a.num_experts) {
                 const int owner = my_id / a.experts_per_rank;
                 if (owner < 32)
@@ -276,7 +289,8 @@ __global__ void __launch_bounds__(kDispatchThreads)
         lo = __reduce_or_sync(kFull, lo);
         hi = __reduce_or_sync(kFull, hi);
         const uint64_t m = ((((uint64_t)hi) << 32) | lo) & a.active;
-        if (chunk == 0 && lane == 0)
+        if (chunk == 0 && lane == 0 &&
+            EP_IN_BOUNDS(a.chk, kSiteRouteWrite, a.route_mask + slot, 8, a.route_mask, n_slots * 8))
             a.route_mask[slot] = m;
 
         // ---- id rows of this slot in all destination ranks (first chunk's item)
@@ -299,7 +313,9 @@ __global__ void __launch_bounds__(kDispatchThreads)
                     if (!((m >> d) & 1u))
                         v = make_int4(EP_INVALID_EXPERT_ID, EP_INVALID_EXPERT_ID,
                                       EP_INVALID_EXPERT_ID, EP_INVALID_EXPERT_ID);
-                    *reinterpret_cast<int4 *>(ids_slot + d * a.ids_stride + 4 * q) = v;
+                    int32_t *p = ids_slot + d * a.ids_stride + 4 * q;
+                    if (EP_IN_BOUNDS(a.chk, kSiteRecvIds, p, 16, a.recv_ids + d * a.ids_stride, n_slots * K * 4))
+                        *reinterpret_cast<int4 *>(p) = v;
                 }
             }
         } else {
@@ -312,7 +328,9 @@ __global__ void __launch_bounds__(kDispatchThreads)
                 if (i < n) {
                     if (!((m >> d) & 1u))
                         v = EP_INVALID_EXPERT_ID;
-                    ids_slot[d * a.ids_stride + k] = v;
+                    int32_t *p = ids_slot + d * a.ids_stride + k;
+                    if (EP_IN_BOUNDS(a.chk, kSiteRecvIds, p, 4, a.recv_ids + d * a.ids_stride, n_slots * K * 4))
+                        *p = v;
                 }
             }
         }
@@ -327,7 +345,8 @@ __global__ void __launch_bounds__(kDispatchThreads)
 #pragma unroll
             for (int j = 0; j < kVpl; ++j) {
                 const int idx = c0 + j * 32 + lane;
-                if (idx < nvec)
+                if (idx < nvec && EP_IN_BOUNDS(a.chk, kSiteRecvHidden, dst + VB * (long long)idx, VB,
+                                               a.recv_hidden + d * a.hidden_stride, n_slots * a.row_bytes))
                     RV::store(dst + VB * (long long)idx, v[j]);
             }
         }
@@ -339,19 +358,30 @@ __global__ void __launch_bounds__(kDispatchThreads)
             const float *ssrc = a.scale[s] + (long long)t * a.G;
             float *sdst = a.recv_scale + slot * a.G;
             for (int j = lane; j < a.G; j += 32) {
-                const float x = ssrc[j];
+                float x = 0.0f;
+                if (EP_IN_BOUNDS(a.chk, kSiteSrcScale, ssrc + j, 4, a.scale[s], (long long)a.num_tokens[s] * a.G * 4))
+                    x = ssrc[j];
                 for (uint64_t mm = m; mm; mm &= mm - 1) {
                     const int d = __ffsll((long long)mm) - 1;
-                    sdst[d * a.scale_stride + j] = x;
+                    float *p = sdst + d * a.scale_stride + j;
+                    if (EP_IN_BOUNDS(a.chk, kSiteRecvScale, p, 4, a.recv_scale + d * a.scale_stride,
+                                     n_slots * a.G * 4))
+                        *p = x;
                 }
             }
         }
         if (a.has_weights && lane < K) {
-            const float w = a.weights[s][(long long)t * K + lane];
+            const float *wp = a.weights[s] + (long long)t * K + lane;
+            float w = 0.0f;
+            if (EP_IN_BOUNDS(a.chk, kSiteSrcWeights, wp, 4, a.weights[s], (long long)a.num_tokens[s] * K * 4))
+                w = *wp;
             float *wdst = a.recv_weights + slot * K + lane;
             for (uint64_t mm = m; mm; mm &= mm - 1) {
                 const int d = __ffsll((long long)mm) - 1;
-                wdst[d * a.weights_stride] = w;
+                float *p = wdst + d * a.weights_stride;
+                if (EP_IN_BOUNDS(a.chk, kSiteRecvWeights, p, 4, a.recv_weights + d * a.weights_stride,
+                                 n_slots * K * 4))
+                    *p = w;
             }
         }
     }
@@ -400,7 +430,9 @@ __global__ void __launch_bounds__(kCombineMaxThreads)
         const int v0 = chunk * (nthr * kV) + threadIdx.x;
         if (v0 >= nvec)
             continue;
-        const uint64_t m = a.route_mask[slot];
+        uint64_t m = 0;
+        if (EP_IN_BOUNDS(a.chk, kSiteRouteRead, a.route_mask + slot, 8, a.route_mask, (long long)a.ep * a.T * 8))
+            m = a.route_mask[slot];
         const long long row = slot * row_bytes;  // byte offset of the slot's row in a rank's buffer
 
         float acc[kV][kH][kEpv];
@@ -415,6 +447,13 @@ __global__ void __launch_bounds__(kCombineMaxThreads)
         uint64_t mm = m;
         while (mm) {
             typename RV::T x[kCombineBatch][kV];
+#if EP_CHECKED
+#pragma unroll
+            for (int r = 0; r < kCombineBatch; ++r)
+#pragma unroll
+                for (int j = 0; j < kV; ++j)
+                    x[r][j] = typename RV::T{};
+#endif
             int nb = 0;
 #pragma unroll
             for (int r = 0; r < kCombineBatch; ++r) {
@@ -425,7 +464,8 @@ __global__ void __launch_bounds__(kCombineMaxThreads)
 #pragma unroll
                     for (int j = 0; j < kV; ++j) {
                         const int v = v0 + j * nthr;
-                        if (v < nvec)
+                        if (v < nvec && EP_IN_BOUNDS(a.chk, kSiteCombineIn, base + VB * (long long)v, VB, a.eo[d],
+                                                     (long long)a.ep * a.T * row_bytes))
                             x[r][j] = RV::load(base + VB * (long long)v);
                     }
                     nb = r + 1;
@@ -456,7 +496,9 @@ __global__ void __launch_bounds__(kCombineMaxThreads)
 #pragma unroll
                 for (int h = 0; h < kH; ++h)
                     set_half16(o, h, Codec::narrow(acc[j][h]));
-                RV::store(out + VB * (long long)v, o);
+                if (EP_IN_BOUNDS(a.chk, kSiteCombineOut, out + VB * (long long)v, VB, a.out[s],
+                                 (long long)a.num_tokens[s] * row_bytes))
+                    RV::store(out + VB * (long long)v, o);
             }
         }
     }

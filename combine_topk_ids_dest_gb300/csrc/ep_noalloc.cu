@@ -43,6 +43,7 @@ struct NoallocRouteArgs {
     uint64_t *route;                  // device address of g_noalloc_route
     uint64_t active;
     int ep, num_experts, experts_per_rank, top_k, T;
+    epk::CheckCtx chk;
 };
 
 // One thread per slot s*T+t: the set of active ranks owning one of the
@@ -59,13 +60,18 @@ __global__ void noalloc_route_kernel(const __grid_constant__ NoallocRouteArgs a)
         if (t < a.num_tokens[s]) {
             const int32_t *row = a.ids[s] + (long long)t * a.top_k;
             for (int k = 0; k < a.top_k; ++k) {
-                const int e = row[k];
+                int e = -1;
+                if (EP_IN_BOUNDS(a.chk, epk::kSiteNoallocIds, row + k, 4, a.ids[s],
+                                 (long long)a.num_tokens[s] * a.top_k * 4))
+                    e = row[k];
                 if (e >= 0 && e < a.num_experts)
                     m |= 1ULL << (e / a.experts_per_rank);
             }
             m &= a.active;
         }
-        a.route[slot] = m;
+        if (EP_IN_BOUNDS(a.chk, epk::kSiteNoallocRoute, a.route + slot, 8, a.route,
+                         (long long)EP_NOALLOC_MAX_SLOTS * 8))
+            a.route[slot] = m;
     }
 }
 
@@ -182,6 +188,13 @@ extern "C" ep_status ep_combine_noalloc(int ep_size, int num_experts, int top_k,
     c.T = tokens_per_rank;
     c.H = hidden;
     c.ctype = EP_DTYPE_BF16;
+    unsigned long long *rec = nullptr;
+#if EP_CHECKED
+    rec = epk::check_record();
+    if (!rec)
+        return EP_ERR_CUDA;
+#endif
+    a.chk = c.chk = epk::check_ctx(rec);
 
     const long long n_slots = (long long)ep_size * tokens_per_rank;
     if (n_slots == 0)
@@ -198,5 +211,8 @@ extern "C" ep_status ep_combine_noalloc(int ep_size, int num_experts, int top_k,
     ce = epk::launch_combine(c, s);  // the library's combine, reading the static routing array
     if (ce != cudaSuccess)
         return epk::set_error(EP_ERR_CUDA, "ep_combine_noalloc combine launch: %s", cudaGetErrorString(ce));
+    st = epk::check_after(rec, s, "ep_combine_noalloc");
+    if (st != EP_OK)
+        return st;
     return epk::set_error(EP_OK, "");
 }

@@ -216,8 +216,11 @@ class EpComm:
                                     ctypes.cast(c_counts, ctypes.c_void_p).value, rt,
                                     _mask_value(active_rank_mask), addr(eplb_ptrs), eplb_bytes)
         with torch.cuda.device(self.device):
-            check(self._L.ep_dispatch_ex(self._h, ctypes.byref(args),
-                                         ctypes.c_void_p(_stream_ptr(self.device)), ctypes.byref(res)))
+            st = self._L.ep_dispatch_ex(self._h, ctypes.byref(args),
+                                        ctypes.c_void_p(_stream_ptr(self.device)), ctypes.byref(res))
+        if st == _lib.EP_ERR_DEVICE_CHECK:  # checked build: the dispatch happened; keep its state
+            self._counts, self._T = counts, res.tokens_per_rank
+        check(st)
         T = res.tokens_per_rank
         self._counts, self._T = counts, T
         hs = self._rank_views("hidden", res.recv_hidden, T, H, self.dtype)
@@ -292,10 +295,13 @@ class EpComm:
             for s in range(ep):
                 self._check_rank_tensor("output", output[s], s, self._counts[s], H, self.combine_dtype)
         with torch.cuda.device(self.device):
-            check(self._L.ep_combine(self._h, ptr_array(eo_ptrs) if eo_ptrs is not None else None,
-                                     ptr_array([o.data_ptr() for o in output]),
-                                     _mask_value(active_rank_mask),
-                                     ctypes.c_void_p(_stream_ptr(self.device))))
+            st = self._L.ep_combine(self._h, ptr_array(eo_ptrs) if eo_ptrs is not None else None,
+                                    ptr_array([o.data_ptr() for o in output]),
+                                    _mask_value(active_rank_mask),
+                                    ctypes.c_void_p(_stream_ptr(self.device)))
+        if st == _lib.EP_ERR_DEVICE_CHECK:  # checked build: the combine happened
+            self._counts = None
+        check(st)
         self._counts = None
         return list(output)
 

@@ -40,6 +40,18 @@
  * state on the host before it launches anything, and returns a status;
  * ep_last_error() gives a message. GPU work is queued on the given stream
  * (NULL = the legacy default stream) and is asynchronous to the host.
+ *
+ * Checked build (libep_gb300_checked.so, compiled with EP_CHECKED=1; same
+ * ABI): the kernels test every global access against the extent this
+ * header gives its buffer, skip any access outside and record it; after
+ * its launches each call waits for its stream and returns
+ * EP_ERR_DEVICE_CHECK (with the first access's buffer and offset in
+ * ep_last_error) if anything was recorded. The call's other effects
+ * (state, results of the accesses that were inside) stand. Inside a stream
+ * capture the wait is skipped and the record is reported by the next call
+ * outside one. All calls of the library share one record per device, so
+ * overlapping work on two streams may report the other's access. It is
+ * for testing: slower, and synchronous.
  */
 #ifndef EP_GB300_H
 #define EP_GB300_H
@@ -57,7 +69,8 @@ typedef enum {
     EP_ERR_STATE = 2,       /* dispatch while one is pending, combine without dispatch */
     EP_ERR_CUDA = 3,        /* a CUDA runtime call failed (message has the CUDA error) */
     EP_ERR_OOM = 4,         /* workspace allocation failed */
-    EP_ERR_UNSUPPORTED = 5  /* no sm_103 device current */
+    EP_ERR_UNSUPPORTED = 5, /* no sm_103 device current */
+    EP_ERR_DEVICE_CHECK = 6 /* checked build only (below): a kernel access fell outside its buffer */
 } ep_status;
 
 typedef enum {

@@ -29,7 +29,8 @@ def test_header_and_exports_agree():
 
 def test_library_is_built_for_sm103a():
     path = _lib.load()._name
-    assert os.path.basename(path) == "libep_gb300.so"
+    assert os.path.basename(path) == os.path.basename(_lib.lib_path())
+    assert os.path.basename(path) in ("libep_gb300.so", "libep_gb300_checked.so")
     assert os.path.dirname(path).endswith(os.path.join("combine_topk_ids_dest_gb300", "_build"))
 
 
@@ -182,3 +183,40 @@ def test_null_config_and_args_rejected():
     assert L.ep_create_ex(None, None, 0, ctypes.byref(h)) == ep.EP_ERR_INVALID_ARG
     res = _lib.EpDispatchResultC()
     assert L.ep_dispatch_ex(None, None, None, ctypes.byref(res)) == ep.EP_ERR_INVALID_ARG
+
+
+def test_device_check_status_matches_header():
+    text = open(HEADER).read()
+    assert re.search(r"EP_ERR_DEVICE_CHECK\s*=\s*6\b", text)
+    assert _lib.EP_ERR_DEVICE_CHECK == 6 and _lib.STATUS_NAMES[6] == "EP_ERR_DEVICE_CHECK"
+
+
+def test_check_sites_match_the_kernels_enum():
+    internal = os.path.join(os.path.dirname(HEADER), "..", "combine_topk_ids_dest_gb300", "csrc", "ep_internal.h")
+    body = re.search(r"enum CheckSite \{(.*?)\};", open(internal).read(), flags=re.S).group(1)
+    names = [n.split("=")[0].strip() for n in body.split(",") if n.strip()]
+    assert names[-1] == "kNumSites"
+    snake = [re.sub(r"(?<!^)([A-Z])", r"_\1", n[len("kSite"):]).lower() for n in names[:-1]]
+    assert tuple(snake) == _lib.CHECK_SITES
+
+
+def test_checked_build_loads_and_exports_the_abi():
+    # In a child process: the loader picks the checked library under EP_GB300_CHECKED=1.
+    import subprocess
+    import sys
+    code = ("import os; from combine_topk_ids_dest_gb300 import _lib; L = _lib.load(); "
+            "print(os.path.basename(L._name)); "
+            "print(all(hasattr(L, n) for n in _lib.EXPORTS)); "
+            "print(L.ep_checked_trim_extent(99, 0), L.ep_checked_trim_extent(0, -1), "
+            "L.ep_checked_trim_extent(3, 64), L.ep_checked_trim_extent(-1, 0))")
+    root = os.path.dirname(os.path.dirname(HEADER))
+    r = subprocess.run([sys.executable, "-c", code], cwd=root, capture_output=True, text=True, timeout=600,
+                       env=dict(os.environ, EP_GB300_CHECKED="1"))
+    assert r.returncode == 0, r.stderr[-3000:]
+    lines = r.stdout.split()
+    assert lines[0] == "libep_gb300_checked.so" and lines[1] == "True"
+    assert lines[2:] == ["1", "1", "0", "0"]  # bad site, negative bytes, then two valid calls
+
+
+def test_normal_build_has_no_test_hook():
+    assert not hasattr(_lib.load(), "ep_checked_trim_extent") or _lib.checked()
