@@ -31,6 +31,8 @@
 // Nothing here is a dense contraction; both kernels are bound by HBM
 // bandwidth, so the design is about coalesced 16- and 32-byte accesses and
 // enough bytes in flight per SM. Launch shapes come from sweeps on GB300.
+#include <atomic>
+
 #include "ep_internal.h"
 
 namespace epk {
@@ -518,19 +520,21 @@ int combine_threads(int nvec)
     return 64;
 }
 
+// SM count of the current device, looked up once per device (host threads
+// may launch concurrently: the cache is atomic).
 int sm_count()
 {
-    static int cached[64] = {0};
+    static std::atomic<int> cached[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
         return 152;
-    if (!cached[dev]) {
-        int n = 0;
+    int n = cached[dev].load(std::memory_order_relaxed);
+    if (n == 0) {
         if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
             n = 152;
-        cached[dev] = n;
+        cached[dev].store(n, std::memory_order_relaxed);
     }
-    return cached[dev];
+    return n;
 }
 
 }  // namespace

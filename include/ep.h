@@ -41,6 +41,11 @@
  * ep_last_error() gives a message. GPU work is queued on the given stream
  * (NULL = the legacy default stream) and is asynchronous to the host.
  *
+ * Threads: calls on different handles may come from different host threads
+ * at once; calls on one handle must not overlap (a handle holds the state
+ * of its pending dispatch). ep_last_error() is per thread. Every call works
+ * on the current CUDA device, which must be the handle's.
+ *
  * Checked build (libep_gb300_checked.so, compiled with EP_CHECKED=1; same
  * ABI): the kernels test every global access against the extent this
  * header gives its buffer, skip any access outside and record it; after

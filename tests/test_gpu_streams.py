@@ -62,6 +62,59 @@ def test_two_handles_on_two_streams(cuda_device):
             c.destroy()
 
 
+def test_handles_used_from_two_host_threads(cuda_device):
+    """Two host threads, each with its own handle and stream, run rounds at the
+    same time (ctypes calls release the interpreter lock, so the library's
+    host code runs concurrently); each thread's last round matches the oracle."""
+    import threading
+    wls = [workloads.EpWorkload(name="ta", ep_size=4, num_experts=16, top_k=2, hidden=2048, dtype="bf16",
+                                capacity=96, runtime_max=None, counts=("uniform", 0, 96), seed=73),
+           workloads.EpWorkload(name="tb", ep_size=32, num_experts=128, top_k=8, hidden=256, dtype="bf16",
+                                capacity=24, runtime_max=None, counts=("uniform", 0, 24),
+                                dropped_ranks=(5,), seed=74)]
+    inps = [workloads.make_inputs(wl) for wl in wls]
+    got, errors = [None, None], []
+
+    def worker(i):
+        try:
+            wl, inp = wls[i], inps[i]
+            comm = EpComm(wl.ep_size, wl.num_experts, wl.top_k, wl.hidden, wl.capacity,
+                          enable_rank_mask=wl.enable_rank_mask, device=cuda_device)
+            st = torch.cuda.Stream(cuda_device)
+            try:
+                with torch.cuda.stream(st):
+                    h, ids, w = (to_dev(inp.hidden, cuda_device), to_dev(inp.topk_ids, cuda_device),
+                                 to_dev(inp.topk_weights, cuda_device))
+                    rows = torch.arange(wl.ep_size * wl.tokens_per_rank)
+                    eo = [workloads.expert_output_rows(EO_SEED, d, rows, wl.hidden).to(cuda_device)
+                          for d in range(wl.ep_size)]
+                    mask = inp.active_rank_mask if wl.enable_rank_mask else None
+                    for _ in range(5):
+                        res = comm.dispatch(h, ids, w, active_rank_mask=mask)
+                        out = comm.combine(eo, active_rank_mask=mask)
+                    ids_out = [x.cpu() for x in res.topk_ids]
+                    got[i] = (ids_out, [x.cpu() for x in out])
+                st.synchronize()
+            finally:
+                comm.destroy()
+        except Exception as e:  # reported by the main thread
+            errors.append(e)
+
+    threads = [threading.Thread(target=worker, args=(i,)) for i in range(2)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join(timeout=600)
+    assert not errors, errors
+    for i, inp in enumerate(inps):
+        disp, out = oracle_round(inp)
+        ids_out, outs = got[i]
+        for d in range(inp.wl.ep_size):
+            np.testing.assert_array_equal(ids_out[d].numpy(), disp.recv_ids[d])
+        for s in range(inp.wl.ep_size):
+            np.testing.assert_array_equal(bf16_bits(outs[s]), out[s])
+
+
 def test_binding_rejects_wrong_tensors(cuda_device):
     comm = EpComm(2, 4, 2, 64, 8, device=cuda_device)
     try:
