@@ -25,7 +25,7 @@ STATUS_NAMES = {0: "EP_OK", 1: "EP_ERR_INVALID_ARG", 2: "EP_ERR_STATE", 3: "EP_E
 # Access sites of the checked build (enum CheckSite in csrc/ep_internal.h).
 CHECK_SITES = ("src_hidden", "src_ids", "src_scale", "src_weights", "recv_hidden", "recv_ids",
                "recv_scale", "recv_weights", "route_write", "eplb_src", "eplb_dst", "route_read",
-               "combine_in", "combine_out", "noalloc_ids", "noalloc_route")
+               "combine_in", "combine_out", "noalloc_ids", "noalloc_route", "dev_counts", "live_counts")
 
 EP_DTYPE_BF16 = 0
 EP_DTYPE_FP8_E4M3 = 1
@@ -69,7 +69,7 @@ class EpDispatchArgsC(ctypes.Structure):
                 ("topk_ids", ctypes.c_void_p), ("topk_weights", ctypes.c_void_p),
                 ("num_tokens", ctypes.c_void_p), ("runtime_max_tokens_per_rank", ctypes.c_int),
                 ("active_rank_mask", ctypes.c_uint64), ("eplb_local_stats", ctypes.c_void_p),
-                ("eplb_stats_bytes", ctypes.c_int)]
+                ("eplb_stats_bytes", ctypes.c_int), ("num_tokens_device", ctypes.c_void_p)]
 
 
 class EpError(RuntimeError):

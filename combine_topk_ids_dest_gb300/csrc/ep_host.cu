@@ -22,6 +22,7 @@
 //   recv_weights [ep][ep*C][K] fp32
 //   combine_in   [ep][ep*C][H] bf16
 //   route_mask   [ep*C] uint64
+//   live_counts  [ep] int32  (token counts of a dispatch with device-side counts)
 //   eplb_stats   [ep][eplb_stats_max_bytes]  (the gathered eplb_local_stats)
 // A step with tokens_per_rank T uses the first ep*T rows of each region, so
 // receive row s*T+t of rank d sits at region base + d*stride + (s*T+t)*row.
@@ -48,11 +49,12 @@ struct ep_handle {
     uint8_t *ws;
     size_t ws_bytes;
     bool owns_ws;
-    size_t off_hidden, off_scale, off_ids, off_weights, off_comb, off_mask, off_eplb;
+    size_t off_hidden, off_scale, off_ids, off_weights, off_comb, off_mask, off_counts, off_eplb;
     size_t st_hidden, st_scale, st_ids, st_weights, st_comb;  // bytes per rank region
 
     // state of the pending dispatch
     bool pending;
+    bool dev_counts;  // its token counts are device-side (live_counts region)
     int T;
     uint64_t mask;
     int32_t counts[EP_MAX_EP_SIZE];
@@ -90,7 +92,7 @@ uint64_t full_mask(int ep) { return ep >= 64 ? ~0ULL : ((1ULL << ep) - 1); }
 
 struct Layout {
     int elem_bytes, row_bytes, scale_cols, combine_elem;
-    size_t off_hidden, off_scale, off_ids, off_weights, off_comb, off_mask, off_eplb, total;
+    size_t off_hidden, off_scale, off_ids, off_weights, off_comb, off_mask, off_counts, off_eplb, total;
     size_t st_hidden, st_scale, st_ids, st_weights, st_comb;
 };
 
@@ -187,6 +189,8 @@ ep_status plan(const ep_config *cfg, Layout *L)
     off += L->st_comb * ep;
     L->off_mask = off;
     off += align256(rows * sizeof(uint64_t));
+    L->off_counts = off;
+    off += align256((size_t)ep * sizeof(int32_t));
     L->off_eplb = off;
     off += align256((size_t)ep * (size_t)cfg->eplb_stats_max_bytes);
     L->total = off < 256 ? 256 : off;
@@ -260,6 +264,7 @@ ep_status make_handle(const ep_config *cfg, void *ws, size_t ws_bytes, bool own,
     h->off_weights = L.off_weights;
     h->off_comb = L.off_comb;
     h->off_mask = L.off_mask;
+    h->off_counts = L.off_counts;
     h->off_eplb = L.off_eplb;
     h->st_hidden = L.st_hidden;
     h->st_scale = L.st_scale;
@@ -267,6 +272,7 @@ ep_status make_handle(const ep_config *cfg, void *ws, size_t ws_bytes, bool own,
     h->st_weights = L.st_weights;
     h->st_comb = L.st_comb;
     h->pending = false;
+    h->dev_counts = false;
     h->T = 0;
     h->mask = 0;
     for (int d = 0; d < ep; ++d) {
@@ -335,7 +341,7 @@ const char *epk::check_site_name(int site)
         "dispatch: receive scale row", "dispatch: receive weight row", "dispatch: routing state",
         "dispatch: eplb_local_stats", "dispatch: gathered eplb stats", "combine: routing state",
         "combine: expert output row", "combine: output row", "ep_combine_noalloc: id row",
-        "ep_combine_noalloc: routing scratch"};
+        "ep_combine_noalloc: routing scratch", "dispatch: device token counts", "live token counts"};
     return (site >= 0 && site < kNumSites) ? names[site] : "unknown site";
 }
 
@@ -499,6 +505,7 @@ ep_status ep_dispatch(ep_handle *h, const void *const *hidden, const float *cons
     args.active_rank_mask = active_rank_mask;
     args.eplb_local_stats = nullptr;
     args.eplb_stats_bytes = 0;
+    args.num_tokens_device = nullptr;
     return ep_dispatch_ex(h, &args, stream, out);
 }
 
@@ -532,6 +539,8 @@ ep_status ep_dispatch_ex(ep_handle *h, const ep_dispatch_args *args, void *strea
     if (hidden_scale && h->scale_cols == 0)
         return fail(EP_ERR_INVALID_ARG, "hidden_scale given but the handle has no scale columns "
                                         "(hidden %% %d != 0 or scale_cols = 0)", EP_SCALE_GROUP);
+    if (args->num_tokens_device && !aligned(args->num_tokens_device, 4))
+        return fail(EP_ERR_INVALID_ARG, "num_tokens_device is not 4-byte aligned");
     const int eplb_bytes = args->eplb_local_stats ? args->eplb_stats_bytes : 0;
     if (args->eplb_local_stats) {
         if (h->eplb_max_bytes == 0)
@@ -592,6 +601,8 @@ ep_status ep_dispatch_ex(ep_handle *h, const ep_dispatch_args *args, void *strea
     a.has_weights = topk_weights ? 1 : 0;
     a.eplb_dst = h->ws + h->off_eplb;
     a.eplb_bytes = eplb_bytes;
+    a.dev_counts = args->num_tokens_device;
+    a.live_counts = args->num_tokens_device ? reinterpret_cast<int32_t *>(h->ws + h->off_counts) : nullptr;
     unsigned long long *rec = nullptr;
 #if EP_CHECKED
     rec = epk::check_record();
@@ -607,6 +618,7 @@ ep_status ep_dispatch_ex(ep_handle *h, const ep_dispatch_args *args, void *strea
         return fail(EP_ERR_CUDA, "dispatch launch: %s", cudaGetErrorString(ce));
 
     h->pending = true;
+    h->dev_counts = args->num_tokens_device != nullptr;
     h->T = T;
     h->mask = mask;
     for (int s = 0; s < h->ep; ++s)
@@ -679,6 +691,7 @@ ep_status ep_combine(ep_handle *h, const void *const *expert_output, void *const
         a.out[s] = output[s];
     }
     a.route_mask = reinterpret_cast<const uint64_t *>(h->ws + h->off_mask);
+    a.live_counts = h->dev_counts ? reinterpret_cast<const int32_t *>(h->ws + h->off_counts) : nullptr;
     a.ep = h->ep;
     a.T = h->T;
     a.H = h->hidden;

@@ -28,7 +28,7 @@ enum CheckSite {
     kSiteRecvHidden, kSiteRecvIds, kSiteRecvScale, kSiteRecvWeights,
     kSiteRouteWrite, kSiteEplbSrc, kSiteEplbDst,
     kSiteRouteRead, kSiteCombineIn, kSiteCombineOut,
-    kSiteNoallocIds, kSiteNoallocRoute,
+    kSiteNoallocIds, kSiteNoallocRoute, kSiteDevCounts, kSiteLiveCounts,
     kNumSites
 };
 
@@ -77,7 +77,13 @@ struct DispatchArgs {
     const float *scale[kMaxEp];     // [num_tokens[s], G] or unused
     const int32_t *ids[kMaxEp];     // [num_tokens[s], K]
     const float *weights[kMaxEp];   // [num_tokens[s], K] or unused
-    int num_tokens[kMaxEp];
+    int num_tokens[kMaxEp];         // tokens of rank s; with dev_counts, its maximum
+
+    // Device-side counts (NULL: num_tokens is exact): rank s has
+    // clamp(dev_counts[s], 0, num_tokens[s]) tokens; the kernel stores that
+    // into live_counts[s] for the combine.
+    const int32_t *dev_counts;
+    int32_t *live_counts;
 
     // Destination rank d's receive buffer of each kind starts at base + d*stride
     // (strides in elements of the buffer's type); row r = s*T + t.
@@ -113,6 +119,9 @@ struct CombineArgs {
     int token_offset[kMaxEp + 1];  // prefix sums of num_tokens: live token g of rank s has
                                    // token_offset[s] <= g < token_offset[s+1]
     const uint64_t *route_mask;    // [ep*T], written by the dispatch
+    const int32_t *live_counts;    // NULL, or [ep] device counts the dispatch stored
+                                   // (num_tokens are then maxima: rows past the count
+                                   // are skipped)
     int ep, T, H;
     int ctype;  // element type of eo/out: EP_DTYPE_BF16, EP_DTYPE_FP16 or EP_DTYPE_FP32
 

@@ -252,7 +252,17 @@ __global__ void __launch_bounds__(kDispatchThreads)
         const int c0 = chunk * chunk_vecs;
         const int s = (int)(slot / a.T);
         const int t = (int)(slot - (long long)s * a.T);
-        const bool live = t < a.num_tokens[s];
+        int n_s = a.num_tokens[s];
+        if (a.dev_counts) {  // counts read at run time, clamped to [0, the host maximum]
+            int c = 0;
+            if (EP_IN_BOUNDS(a.chk, kSiteDevCounts, a.dev_counts + s, 4, a.dev_counts, (long long)a.ep * 4))
+                c = a.dev_counts[s];
+            n_s = c < 0 ? 0 : (c < n_s ? c : n_s);
+            if (t == 0 && chunk == 0 && lane == 0 &&
+                EP_IN_BOUNDS(a.chk, kSiteLiveCounts, a.live_counts + s, 4, a.live_counts, (long long)a.ep * 4))
+                a.live_counts[s] = n_s;  // for the combine
+        }
+        const bool live = t < n_s;
 
         // ---- this chunk of the hidden row, loaded before the routing so the
         // two memory round trips overlap (almost every live token is routed)
@@ -428,6 +438,13 @@ __global__ void __launch_bounds__(kCombineMaxThreads)
         }
         const int s = lo;
         const int t = g - a.token_offset[s];
+        if (a.live_counts) {  // device-side counts: rows past the dispatch's count are skipped
+            int c = 0;
+            if (EP_IN_BOUNDS(a.chk, kSiteLiveCounts, a.live_counts + s, 4, a.live_counts, (long long)a.ep * 4))
+                c = a.live_counts[s];
+            if (t >= c)
+                continue;
+        }
         const long long slot = (long long)s * a.T + t;
         const int v0 = chunk * (nthr * kV) + threadIdx.x;
         if (v0 >= nvec)

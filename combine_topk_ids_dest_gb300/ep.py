@@ -160,7 +160,8 @@ class EpComm:
                  hidden_states_scale: Optional[Sequence[torch.Tensor]] = None,
                  runtime_max_tokens_per_rank: Optional[int] = None,
                  eplb_local_stats: Optional[Sequence[torch.Tensor]] = None,
-                 active_rank_mask=None) -> EpDispatchResult:
+                 active_rank_mask=None,
+                 num_tokens_device: Optional[torch.Tensor] = None) -> EpDispatchResult:
         """Scatter each rank's tokens to the ranks holding one of their top-k experts.
 
         Per rank s: ``hidden_states[s]`` [n_s, hidden] (dtype of the
@@ -169,6 +170,13 @@ class EpComm:
         fp32 [n_s, scale_cols]. Weights and scales are all-or-none over ranks.
         ``eplb_local_stats[s]`` (optional, every rank the same dtype and shape,
         a multiple of 4 bytes) is gathered into ``eplb_global_stats``.
+
+        ``num_tokens_device`` (optional, int32 CUDA tensor of ``ep_size``
+        counts) is read by the kernels when they run: rank s then has
+        ``min(max(num_tokens_device[s], 0), n_s)`` tokens, ``n_s`` (the row
+        count of its tensors) being its maximum. For CUDA graphs whose token
+        counts change between replays; the following combine() writes only
+        the first count rows of each output.
         """
         self._live()
         ep, K, H = self.ep_size, self.top_k, self.hidden
@@ -202,6 +210,14 @@ class EpComm:
             if hidden_states_scale is not None:
                 self._check_rank_tensor("hidden_states_scale", hidden_states_scale[s], s, n, G,
                                         torch.float32)
+        dev_counts_ptr = None
+        if num_tokens_device is not None:
+            t = num_tokens_device
+            if t.dtype is not torch.int32 or not t.is_cuda or t.get_device() != self._dev_index \
+                    or t.numel() != ep or not t.is_contiguous():
+                raise ValueError(f"num_tokens_device must be a contiguous int32 tensor of {ep} counts "
+                                 f"on {self.device}")
+            dev_counts_ptr = t.data_ptr()
         c_counts = (ctypes.c_int32 * ep)(*counts)
         res = _lib.EpDispatchResultC()
         rt = -1 if runtime_max_tokens_per_rank is None else int(runtime_max_tokens_per_rank)
@@ -214,7 +230,8 @@ class EpComm:
         addr = lambda a: ctypes.cast(a, ctypes.c_void_p).value if a is not None else None
         args = _lib.EpDispatchArgsC(addr(keep[0]), addr(keep[1]), addr(keep[2]), addr(keep[3]),
                                     ctypes.cast(c_counts, ctypes.c_void_p).value, rt,
-                                    _mask_value(active_rank_mask), addr(eplb_ptrs), eplb_bytes)
+                                    _mask_value(active_rank_mask), addr(eplb_ptrs), eplb_bytes,
+                                    dev_counts_ptr)
         with torch.cuda.device(self.device):
             st = self._L.ep_dispatch_ex(self._h, ctypes.byref(args),
                                         ctypes.c_void_p(_stream_ptr(self.device)), ctypes.byref(res))

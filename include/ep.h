@@ -135,7 +135,16 @@ typedef struct {
  * device pointer to rank r's eplb_stats_bytes bytes of expert-load
  * statistics (4-byte aligned; every rank passes the same size), gathered
  * into ep_dispatch_result.eplb_global_stats by the same launch
- * (MoEEpCommunication.dispatch, parameter eplb_local_stats). */
+ * (MoEEpCommunication.dispatch, parameter eplb_local_stats).
+ * num_tokens_device: NULL, or a device int32 [ep_size] array the kernels
+ * read when they run: rank s then has min(max(num_tokens_device[s], 0),
+ * num_tokens[s]) tokens, and num_tokens (host) gives each rank's maximum
+ * (its source tensors hold that many rows). This lets one captured CUDA
+ * graph serve steps whose token counts change: the caller writes the new
+ * counts into the array before each replay. The routing, the receive rows
+ * and the combine all follow the device counts; the ep_combine that follows
+ * writes only the first count rows of each output. (An extension for CUDA
+ * graphs; the pages' dispatch takes counts from its tensors' shapes.) */
 typedef struct {
     const void *const *hidden;
     const float *const *hidden_scale;
@@ -146,6 +155,7 @@ typedef struct {
     uint64_t active_rank_mask;
     const void *const *eplb_local_stats;
     int eplb_stats_bytes;
+    const int32_t *num_tokens_device;
 } ep_dispatch_args;
 
 /* 1 when the current CUDA device can run this library (compute capability
@@ -155,8 +165,9 @@ int ep_is_supported(void);
 
 /* Bytes of device workspace a handle with these parameters needs: for every
  * rank, receive buffers and a bf16 combine-input buffer of ep_size *
- * max_tokens_per_rank rows, plus 8 bytes of routing state per slot.
- * Validates the parameters like ep_create. */
+ * max_tokens_per_rank rows, plus 8 bytes of routing state per slot and a
+ * 256-byte block for the live token counts. Validates the parameters like
+ * ep_create. */
 ep_status ep_workspace_size(int ep_size, int num_experts, int top_k, int hidden,
                             int max_tokens_per_rank, ep_dtype dtype, size_t *bytes);
 
@@ -214,9 +225,10 @@ ep_status ep_dispatch(ep_handle *h, const void *const *hidden, const float *cons
                       uint64_t active_rank_mask, void *stream, ep_dispatch_result *out);
 
 /* ep_dispatch with its arguments in a struct, plus the eplb_local_stats
- * all-gather. Same checks and errors; additionally EP_ERR_INVALID_ARG when
- * stats are given to a handle without eplb capacity, exceed it, are not a
- * multiple of 4 bytes, or are missing for some rank. */
+ * all-gather and device-side token counts. Same checks and errors;
+ * additionally EP_ERR_INVALID_ARG when stats are given to a handle without
+ * eplb capacity, exceed it, are not a multiple of 4 bytes, or are missing
+ * for some rank, or when num_tokens_device is not 4-byte aligned. */
 ep_status ep_dispatch_ex(ep_handle *h, const ep_dispatch_args *args, void *stream,
                          ep_dispatch_result *out);
 
@@ -235,6 +247,8 @@ ep_status ep_get_combine_input_buffer(ep_handle *h, int rank, void **out);
  *                  backend buffer), 16-byte aligned; only routed rows are read.
  *  output[s]       device [num_tokens[s], hidden] of the combine dtype, 16-byte
  *                  aligned, caller-owned; may be NULL when num_tokens[s] == 0.
+ *                  After a dispatch with num_tokens_device, num_tokens[s] is the
+ *                  maximum and only the rows below the device count are written.
  *  active_rank_mask  must equal the dispatch's (when masking is enabled).
  * output[s][t] = round( sum over routed ranks d ascending of expert_output[d]
  * [s*tokens_per_rank + t] ) with an fp32 accumulator from +0.0 and one

@@ -54,7 +54,7 @@ def test_workspace_size_formula(ep_size, E, K, H, C, dt):
     elem = 2 if dt == 0 else 1
     G = H // 128 if H % 128 == 0 else 0
     want = ep_size * (_align(rows * H * elem) + _align(rows * G * 4) + _align(rows * K * 4) * 2 +
-                      _align(rows * H * 2)) + _align(rows * 8)
+                      _align(rows * H * 2)) + _align(rows * 8) + _align(ep_size * 4)
     assert n == max(want, 256)
 
 
@@ -134,7 +134,8 @@ def test_workspace_size_ex_formula(dtype, elem, scale_cols, G, eplb):
     ep_size, K, H, C = 4, 2, 256, 16
     rows = ep_size * C
     want = ep_size * (_align(rows * H * elem) + _align(rows * G * 4) + _align(rows * K * 4) * 2 +
-                      _align(rows * H * 2)) + _align(rows * 8) + _align(ep_size * eplb)
+                      _align(rows * H * 2)) + _align(rows * 8) + _align(ep_size * 4) + \
+        _align(ep_size * eplb)
     assert n == want
 
 
@@ -144,7 +145,7 @@ def test_workspace_size_ex_combine_dtype(cdt, ce):
     assert st == ep.EP_OK
     rows = 4 * 16
     want = 4 * (_align(rows * 256 * 2) + _align(rows * 2 * 4) + _align(rows * 2 * 4) * 2 +
-                _align(rows * 256 * ce)) + _align(rows * 8)
+                _align(rows * 256 * ce)) + _align(rows * 8) + _align(4 * 4)
     assert n == want
 
 
