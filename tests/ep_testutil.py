@@ -81,9 +81,11 @@ def fill_expert_outputs(comm, T, device, seed=EO_SEED, special=False, caller=Fal
     return outs if caller else None
 
 
-def gpu_round(inp, device, special=False, caller_eo=False, comm=None, keep=False):
+def gpu_round(inp, device, special=False, caller_eo=False, comm=None, keep=False, dev_counts=None):
     """dispatch + (stand-in expert) + combine of ``inp`` through EpComm.
-    Returns host copies of the receive buffers and outputs."""
+    Returns host copies of the receive buffers and outputs. ``dev_counts``
+    (a list of ints) is passed as device-side token counts; the outputs are
+    then cut to the counts clamped to [0, the rank's rows]."""
     from combine_topk_ids_dest_gb300 import EpComm
     wl = inp.wl
     own = comm is None
@@ -96,10 +98,14 @@ def gpu_round(inp, device, special=False, caller_eo=False, comm=None, keep=False
     res = comm.dispatch(to_dev(inp.hidden, device), to_dev(inp.topk_ids, device),
                         to_dev(inp.topk_weights, device),
                         hidden_states_scale=to_dev(inp.scale, device),
-                        runtime_max_tokens_per_rank=wl.runtime_max, active_rank_mask=mask)
+                        runtime_max_tokens_per_rank=wl.runtime_max, active_rank_mask=mask,
+                        num_tokens_device=None if dev_counts is None else
+                        torch.tensor(dev_counts, dtype=torch.int32, device=device))
     T = res.tokens_per_rank
     eo = fill_expert_outputs(comm, T, device, special=special, caller=caller_eo)
     out = comm.combine(eo, active_rank_mask=mask)
+    if dev_counts is not None:
+        out = [o[:clamp_count(c, n)] for o, c, n in zip(out, dev_counts, inp.num_tokens)]
     torch.cuda.synchronize(device)
     host = dict(
         T=T,
@@ -163,3 +169,16 @@ def assert_round_equal(inp, got, disp, out):
             assert got["recv_weights"] is None
     for s in range(wl.ep_size):
         np.testing.assert_array_equal(got["out"][s], out[s], err_msg=f"combine output of rank {s}")
+
+
+def clamp_count(c, n):
+    """A device-side token count as the kernels use it: clamped to [0, n]."""
+    return min(max(int(c), 0), int(n))
+
+
+def cut_inputs(inp, counts):
+    """``inp`` with every rank's tensors cut to its first ``counts[s]`` rows."""
+    import dataclasses
+    cut = lambda lst: None if lst is None else [x[:n] for x, n in zip(lst, counts)]
+    return dataclasses.replace(inp, num_tokens=list(counts), hidden=cut(inp.hidden), scale=cut(inp.scale),
+                               topk_ids=cut(inp.topk_ids), topk_weights=cut(inp.topk_weights))

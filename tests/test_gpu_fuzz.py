@@ -7,7 +7,7 @@ import random
 import pytest
 
 import workloads
-from ep_testutil import assert_round_equal, gpu_round, oracle_round
+from ep_testutil import assert_round_equal, clamp_count, cut_inputs, gpu_round, oracle_round
 
 pytestmark = pytest.mark.gpu
 
@@ -52,3 +52,18 @@ def test_random_geometry(cuda_device, seed):
     got = gpu_round(inp, cuda_device, caller_eo=caller_eo)
     disp, out = oracle_round(inp)
     assert_round_equal(inp, got, disp, out)
+
+
+@pytest.mark.parametrize("seed", range(20))
+def test_random_geometry_device_counts(cuda_device, seed):
+    """The same geometries with device-side token counts drawn in [-2, rows + 2]:
+    the round must equal the oracle's round of the inputs cut to the clamped
+    counts."""
+    wl, caller_eo = _case(seed)
+    inp = workloads.make_inputs(wl)
+    rng = random.Random(5000 + seed)
+    dev = [rng.randint(-2, n + 2) for n in inp.num_tokens]
+    got = gpu_round(inp, cuda_device, caller_eo=caller_eo, dev_counts=dev)
+    cut = cut_inputs(inp, [clamp_count(c, n) for c, n in zip(dev, inp.num_tokens)])
+    disp, out = oracle_round(cut)
+    assert_round_equal(cut, got, disp, out)
