@@ -9,6 +9,11 @@ step's CUDA events (a 256 MB buffer written, then read back so the flush
 leaves no dirty lines behind); the prefill workload's traffic is also far
 larger than L2.
 
+Timing: the round is captured once as one CUDA graph of the two API calls and
+replayed (as a static-shape caller runs it), with CUDA events around each
+replay; a second pass replays the calls as two graphs with an event between
+them for the per-kernel times of the roofline.
+
 Metric: algorithmic bytes per round / round time, in GB/s, and that as a
 fraction of the measured HBM copy bandwidth. Algorithmic bytes per round,
 with N tokens, P routed (token, rank) pairs, payload row H*b bytes, G scale
