@@ -573,7 +573,7 @@ def run_ours(args, rank, world):
 
     # end to end through the public API from pinned host memory
     e2e_steps = max(4, min(args.steps, 20))
-    e2e_ms = run_e2e(comm, inp, wl, dev, mask, e2e_steps)
+    e2e_ms, h2d_bytes, d2h_bytes = run_e2e(comm, inp, wl, dev, mask, e2e_steps)
     local_cpus = gpu_local_cpus(dev)
 
     total_ms, e2e_ms, eager_ms = reduce_max([total_ms, e2e_ms, eager_ms], device=dev)
@@ -605,9 +605,10 @@ def run_ours(args, rank, world):
                      "unit": "GB/s", "frac": per[top]["frac"], "traffic": per[top]["traffic"],
                      "peak_source": peak_src, "kernels": per},
         "e2e": {"value": whole_job_gbs(b["total"], 1, world, e2e_ms), "unit": "GB/s", "ms_per_step": e2e_ms,
-                "h2d_bytes_per_step": b["h2d"], "d2h_bytes_per_step": b["d2h"], "steps": e2e_steps,
-                "path": "pinned host inputs -> H2D -> EpComm.dispatch/combine (C ABI) -> D2H outputs; "
-                        "H2D, kernels and D2H of consecutive steps overlap on three streams",
+                "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes, "steps": e2e_steps,
+                "path": "pinned host inputs (one packed buffer) -> one H2D copy -> EpComm.dispatch/combine "
+                        "(C ABI) -> one D2H copy of the packed outputs; H2D, kernels and D2H of consecutive "
+                        "steps overlap on three streams",
                 "pinned_on": f"{len(local_cpus)} GPU-local CPUs" if local_cpus else "default placement"},
         "eager": {"value": whole_job_gbs(b["total"], args.steps, world, eager_ms), "unit": "GB/s",
                   "ms_per_step": eager_ms / args.steps,
@@ -640,14 +641,15 @@ def run_ours(args, rank, world):
 
 
 def _packed(tensors, device=None, pin=False):
-    """One contiguous buffer holding `tensors` back to back (16-byte aligned
-    offsets) and per-tensor views into it."""
+    """One contiguous buffer holding `tensors` back to back (32-byte aligned
+    offsets, so the library's 32-byte access paths apply to every view) and
+    per-tensor views into it."""
     import math
     offs, off = [], 0
     for t in tensors:
         offs.append(off)
-        off += -(-t.numel() * t.element_size() // 16) * 16
-    buf = torch.empty(max(off, 16), dtype=torch.uint8, device=device, pin_memory=pin)
+        off += -(-t.numel() * t.element_size() // 32) * 32
+    buf = torch.empty(max(off, 32), dtype=torch.uint8, device=device, pin_memory=pin)
     views = []
     for t, o in zip(tensors, offs):
         nb = t.numel() * t.element_size()
@@ -677,7 +679,8 @@ def run_e2e(comm, inp, wl, dev, mask, steps):
     pinned host memory and its outputs copied back, pipelined over three
     streams with two sets of device buffers: step i's host-to-device copy and
     step i-1's device-to-host copy overlap step i's kernels. Returns the
-    mean wall time per step on the device (ms), after `steps` steps."""
+    mean wall time per step on the device (ms), after `steps` steps, and the
+    bytes copied in each direction per step (the packed buffers' sizes)."""
     kinds = [k for k in ("hidden", "topk_ids", "topk_weights", "scale") if getattr(inp, k) is not None]
     # pinned buffers are placed on the memory node of the allocating CPU:
     # allocate them from the GPU's local CPUs
@@ -685,11 +688,16 @@ def run_e2e(comm, inp, wl, dev, mask, steps):
     prev = os.sched_getaffinity(0)
     if local:
         os.sched_setaffinity(0, local)
-    host = {k: _packed(getattr(inp, k), pin=True) for k in kinds}
-    for k in kinds:
-        for v, t in zip(host[k][1], getattr(inp, k)):
-            v.copy_(t)
-    devsets = [{k: _packed(getattr(inp, k), device=dev) for k in kinds} for _ in range(2)]
+    # every input of a step in one pinned buffer (one host-to-device copy per step)
+    flat = [t for k in kinds for t in getattr(inp, k)]
+    split = lambda views: {k: views[i * wl.ep_size:(i + 1) * wl.ep_size] for i, k in enumerate(kinds)}
+    host_buf, host_views = _packed(flat, pin=True)
+    for v, t in zip(host_views, flat):
+        v.copy_(t)
+    devsets = []
+    for _ in range(2):
+        buf, views = _packed(flat, device=dev)
+        devsets.append((buf, split(views)))
     outs = [torch.empty(n, wl.hidden, dtype=torch.bfloat16) for n in inp.num_tokens]
     dev_out = [_packed(outs, device=dev) for _ in range(2)]
     host_out = [_packed(outs, pin=True) for _ in range(2)]
@@ -710,12 +718,11 @@ def run_e2e(comm, inp, wl, dev, mask, steps):
         k = i % 2
         with torch.cuda.stream(s_in):
             s_in.wait_event(in_free[k])
-            for kind in kinds:
-                devsets[k][kind][0].copy_(host[kind][0], non_blocking=True)
+            devsets[k][0].copy_(host_buf, non_blocking=True)
             in_ready[k].record(s_in)
         comp.wait_event(in_ready[k])
         comp.wait_event(out_free[k])
-        v = {kind: devsets[k][kind][1] for kind in kinds}
+        v = devsets[k][1]
         comm.dispatch(v["hidden"], v["topk_ids"], v.get("topk_weights"), hidden_states_scale=v.get("scale"),
                       runtime_max_tokens_per_rank=wl.runtime_max, active_rank_mask=mask)
         in_free[k].record(comp)
@@ -737,7 +744,7 @@ def run_e2e(comm, inp, wl, dev, mask, steps):
     comp.wait_stream(s_out)
     e1.record(comp)
     torch.cuda.synchronize(dev)
-    return e0.elapsed_time(e1) / steps
+    return e0.elapsed_time(e1) / steps, host_buf.numel(), host_out[0][0].numel()
 
 
 def main():
