@@ -76,6 +76,9 @@ class EpComm:
     is the type of the expert outputs combine sums and of its results. The
     workspace is allocated here with torch, at capacity
     ``max_tokens_per_rank``.
+
+    Different communicators may be used from different threads at once; one
+    communicator must not (it holds the state of its pending dispatch).
     """
 
     def __init__(self, ep_size: int, num_experts: int, top_k: int, hidden: int,
