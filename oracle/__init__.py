@@ -39,7 +39,14 @@ SENTINEL_F32_BITS = 0x7FA5A5A5  # a NaN payload nobody writes by accident
 
 
 def build(force: bool = False) -> str:
-    """Compile ep_oracle.c into oracle/_build/libep_oracle.so (gcc, no fast-math)."""
+    """Compile ep_oracle.c into oracle/_build/libep_oracle.so (gcc, no fast-math).
+
+    EP_ORACLE_LIB in the environment names another build to load instead; the
+    mutation test uses it to run the pins against copies of the oracle with
+    planted mistakes."""
+    override = os.environ.get("EP_ORACLE_LIB")
+    if override:
+        return override
     os.makedirs(_BUILD, exist_ok=True)
     if force or not os.path.exists(_SO) or os.path.getmtime(_SO) < os.path.getmtime(_SRC):
         tmp = _SO + f".tmp{os.getpid()}"
