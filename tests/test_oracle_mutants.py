@@ -49,6 +49,11 @@ MUTANTS = [
     ("ids_only_owned", "id_row[k] = topk_ids[s][(long)t * top_k + k];",
      "id_row[k] = (topk_ids[s][(long)t * top_k + k] / (num_experts / ep_size) == d) ? "
      "topk_ids[s][(long)t * top_k + k] : ORACLE_INVALID_EXPERT_ID;"),
+    ("scale_first_column_only", "recv_scale[d][r * scale_cols + j] = scale[s][(long)t * scale_cols + j];",
+     "recv_scale[d][r * scale_cols + j] = scale[s][(long)t * scale_cols + 0];"),
+    ("hidden_previous_row", "recv_hidden[d][r * row_bytes + b] = hidden[s][(long)t * row_bytes + b];",
+     "recv_hidden[d][r * row_bytes + b] = hidden[s][(long)(t > 0 ? t - 1 : 0) * row_bytes + b];"),
+    ("identity_scale_group_interleaved", "int group = h / (hidden / scale_cols);", "int group = h % scale_cols;"),
     ("weights_not_copied", "recv_weights[d][r * top_k + k] = topk_weights[s][(long)t * top_k + k];",
      "recv_weights[d][r * top_k + k] = 0.0f;"),
     ("combine_descending", "                for (int d = 0; d < ep_size; ++d) {\n" + COMBINE_ADD,
