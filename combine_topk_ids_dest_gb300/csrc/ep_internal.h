@@ -70,8 +70,9 @@ static __device__ __noinline__ bool in_bounds(const CheckCtx &c, int site, const
 #endif
 
 // Everything one dispatch launch needs, passed by value as a __grid_constant__
-// kernel parameter (about 2.4 KB), so no host->device copy precedes a launch
-// and the launch can be captured in a CUDA graph as is.
+// kernel parameter (2984 bytes; the combine's block is 1600), so no
+// host->device copy precedes a launch and the launch can be captured in a
+// CUDA graph as is.
 struct DispatchArgs {
     const uint8_t *hidden[kMaxEp];  // source rank s: [num_tokens[s], row_bytes]
     const float *scale[kMaxEp];     // [num_tokens[s], G] or unused
