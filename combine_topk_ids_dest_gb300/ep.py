@@ -15,10 +15,11 @@ import ctypes
 from dataclasses import dataclass
 from typing import List, Optional, Sequence
 
+import numpy as np
 import torch
 
 from . import _lib
-from ._lib import ALL_RANKS, EpError, check, ptr_array
+from ._lib import ALL_RANKS, EpError, check
 
 _DTYPES = {torch.bfloat16: _lib.EP_DTYPE_BF16, torch.float8_e4m3fn: _lib.EP_DTYPE_FP8_E4M3,
            torch.float16: _lib.EP_DTYPE_FP16, torch.float32: _lib.EP_DTYPE_FP32}
@@ -58,6 +59,16 @@ def _mask_value(m) -> int:
             raise ValueError("active_rank_mask must hold one uint64")
         return int(m.reshape(-1)[0].item()) & ALL_RANKS
     return int(m) & ALL_RANKS
+
+
+def _addr_array(ptrs) -> np.ndarray:
+    """Device addresses as a host uint64 array: the layout of the C ABI's
+    arrays of per-rank pointers (0 = NULL) on 64-bit hosts."""
+    return np.array([int(p) if p else 0 for p in ptrs], dtype=np.uint64)
+
+
+def _data(a) -> Optional[int]:
+    return None if a is None else a.ctypes.data
 
 
 def _stream_ptr(device) -> int:
@@ -114,6 +125,7 @@ class EpComm:
         self._h = h
         self._counts: Optional[List[int]] = None
         self._T = 0
+        self._stacked = False
         self._dev_index = self.device.index if self.device.index is not None else torch.cuda.current_device()
         self._views = {}  # (kind, T) -> per-rank views of the workspace
 
@@ -148,6 +160,25 @@ class EpComm:
             raise ValueError(f"{name}[{s}] must be a contiguous [{n}, {cols}] tensor, got "
                              f"{tuple(t.shape)}")
 
+    def _check_stacked(self, name, t, M, cols, dtype):
+        """Checks one stacked operand, [ep_size, M, cols] (M from the tensor when
+        None); returns M."""
+        ep = self.ep_size
+        if not isinstance(t, torch.Tensor) or t.dim() != 3 or t.shape[0] != ep or t.shape[2] != cols \
+                or (M is not None and t.shape[1] != M):
+            want = f"[{ep}, {'M' if M is None else M}, {cols}]"
+            got = tuple(t.shape) if isinstance(t, torch.Tensor) else type(t).__name__
+            raise ValueError(f"{name} must be a stacked {want} tensor like hidden_states, got {got}")
+        if t.dtype is not dtype or not t.is_cuda or t.get_device() != self._dev_index or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous {dtype} tensor on {self.device}")
+        return int(t.shape[1])
+
+    @staticmethod
+    def _stacked_ptrs(t, M, cols):
+        """Device addresses of every rank's rows in a stacked [ep_size, M, cols] tensor."""
+        step = np.uint64(M * cols * t.element_size())
+        return np.uint64(t.data_ptr()) + step * np.arange(t.shape[0], dtype=np.uint64)
+
     def _rank_views(self, kind, ptrs, T, cols, dtype):
         key = (kind, T)
         v = self._views.get(key)
@@ -158,13 +189,13 @@ class EpComm:
         return list(v)
 
     # -- MoEEpCommunication.dispatch ----------------------------------------
-    def dispatch(self, hidden_states: Sequence[torch.Tensor], topk_ids: Sequence[torch.Tensor],
-                 topk_weights: Optional[Sequence[torch.Tensor]] = None, *,
-                 hidden_states_scale: Optional[Sequence[torch.Tensor]] = None,
+    def dispatch(self, hidden_states, topk_ids, topk_weights=None, *,
+                 hidden_states_scale=None,
                  runtime_max_tokens_per_rank: Optional[int] = None,
                  eplb_local_stats: Optional[Sequence[torch.Tensor]] = None,
                  active_rank_mask=None,
-                 num_tokens_device: Optional[torch.Tensor] = None) -> EpDispatchResult:
+                 num_tokens_device: Optional[torch.Tensor] = None,
+                 num_tokens: Optional[Sequence[int]] = None) -> EpDispatchResult:
         """Scatter each rank's tokens to the ranks holding one of their top-k experts.
 
         Per rank s: ``hidden_states[s]`` [n_s, hidden] (dtype of the
@@ -173,6 +204,13 @@ class EpComm:
         fp32 [n_s, scale_cols]. Weights and scales are all-or-none over ranks.
         ``eplb_local_stats[s]`` (optional, every rank the same dtype and shape,
         a multiple of 4 bytes) is gathered into ``eplb_global_stats``.
+
+        Stacked form: every operand may instead be one contiguous tensor with
+        all ranks' rows, ``hidden_states`` [ep_size, M, hidden], ``topk_ids``
+        [ep_size, M, top_k] and so on, and ``num_tokens`` (default M for every
+        rank) gives each rank's count n_s <= M. One tensor is checked per
+        operand instead of one per rank, so a call costs far less host time
+        at large ep_size; the results are the same.
 
         ``num_tokens_device`` (optional, int32 CUDA tensor of ``ep_size``
         counts) is read by the kernels when they run: rank s then has
@@ -183,14 +221,47 @@ class EpComm:
         """
         self._live()
         ep, K, H = self.ep_size, self.top_k, self.hidden
-        if len(hidden_states) != ep or len(topk_ids) != ep:
-            raise ValueError(f"hidden_states and topk_ids need {ep} per-rank tensors")
-        for name, lst in (("topk_weights", topk_weights), ("hidden_states_scale", hidden_states_scale)):
-            if lst is not None and (len(lst) != ep or any(x is None for x in lst)):
-                raise ValueError(f"{name}: every rank passes it or none does "
-                                 "(an empty rank passes an empty tensor)")
-        counts = [int(x.shape[0]) for x in hidden_states]
         G = self.scale_cols
+        stacked = isinstance(hidden_states, torch.Tensor)
+        if stacked:
+            M = self._check_stacked("hidden_states", hidden_states, None, H, self.dtype)
+            if num_tokens is None:
+                counts = [M] * ep
+            else:
+                counts = [int(n) for n in num_tokens]
+                if len(counts) != ep or any(n < 0 or n > M for n in counts):
+                    raise ValueError(f"num_tokens needs {ep} counts in [0, {M}] (the stacked tensors' rows)")
+            self._check_stacked("topk_ids", topk_ids, M, K, torch.int32)
+            for name, t, cols in (("topk_weights", topk_weights, K), ("hidden_states_scale", hidden_states_scale, G)):
+                if t is not None:
+                    self._check_stacked(name, t, M, cols, torch.float32)
+            hp = self._stacked_ptrs(hidden_states, M, H)
+            ip = self._stacked_ptrs(topk_ids, M, K)
+            wp = self._stacked_ptrs(topk_weights, M, K) if topk_weights is not None else None
+            sp = self._stacked_ptrs(hidden_states_scale, M, G) if hidden_states_scale is not None else None
+        else:
+            if num_tokens is not None:
+                raise ValueError("num_tokens goes with stacked tensors; per-rank tensors give their counts by shape")
+            if len(hidden_states) != ep or len(topk_ids) != ep:
+                raise ValueError(f"hidden_states and topk_ids need {ep} per-rank tensors")
+            for name, lst in (("topk_weights", topk_weights), ("hidden_states_scale", hidden_states_scale)):
+                if lst is not None and (len(lst) != ep or any(x is None for x in lst)):
+                    raise ValueError(f"{name}: every rank passes it or none does "
+                                     "(an empty rank passes an empty tensor)")
+            counts = [int(x.shape[0]) for x in hidden_states]
+            for s in range(ep):
+                n = counts[s]
+                self._check_rank_tensor("hidden_states", hidden_states[s], s, n, H, self.dtype)
+                self._check_rank_tensor("topk_ids", topk_ids[s], s, n, K, torch.int32)
+                if topk_weights is not None:
+                    self._check_rank_tensor("topk_weights", topk_weights[s], s, n, K, torch.float32)
+                if hidden_states_scale is not None:
+                    self._check_rank_tensor("hidden_states_scale", hidden_states_scale[s], s, n, G,
+                                            torch.float32)
+            hp = _addr_array([x.data_ptr() for x in hidden_states])
+            ip = _addr_array([x.data_ptr() for x in topk_ids])
+            wp = _addr_array([x.data_ptr() for x in topk_weights]) if topk_weights is not None else None
+            sp = _addr_array([x.data_ptr() for x in hidden_states_scale]) if hidden_states_scale is not None else None
         eplb_ptrs, eplb_bytes, eplb_meta = None, 0, None
         if eplb_local_stats is not None:
             if len(eplb_local_stats) != ep or any(x is None for x in eplb_local_stats):
@@ -202,17 +273,8 @@ class EpComm:
                     raise ValueError(f"eplb_local_stats[{s}] must be a contiguous {first.dtype} "
                                      f"{tuple(first.shape)} tensor on {self.device}")
             eplb_bytes = first.numel() * first.element_size()
-            eplb_ptrs = ptr_array([x.data_ptr() for x in eplb_local_stats])
+            eplb_ptrs = _addr_array([x.data_ptr() for x in eplb_local_stats])
             eplb_meta = (first.dtype, tuple(first.shape))
-        for s in range(ep):
-            n = counts[s]
-            self._check_rank_tensor("hidden_states", hidden_states[s], s, n, H, self.dtype)
-            self._check_rank_tensor("topk_ids", topk_ids[s], s, n, K, torch.int32)
-            if topk_weights is not None:
-                self._check_rank_tensor("topk_weights", topk_weights[s], s, n, K, torch.float32)
-            if hidden_states_scale is not None:
-                self._check_rank_tensor("hidden_states_scale", hidden_states_scale[s], s, n, G,
-                                        torch.float32)
         dev_counts_ptr = None
         if num_tokens_device is not None:
             t = num_tokens_device
@@ -221,28 +283,23 @@ class EpComm:
                 raise ValueError(f"num_tokens_device must be a contiguous int32 tensor of {ep} counts "
                                  f"on {self.device}")
             dev_counts_ptr = t.data_ptr()
-        c_counts = (ctypes.c_int32 * ep)(*counts)
+        c_counts = np.array(counts, dtype=np.int32)
         res = _lib.EpDispatchResultC()
         rt = -1 if runtime_max_tokens_per_rank is None else int(runtime_max_tokens_per_rank)
         if rt < -1:
             raise ValueError("runtime_max_tokens_per_rank must be >= 0")
-        keep = (ptr_array([x.data_ptr() for x in hidden_states]),
-                ptr_array([x.data_ptr() for x in hidden_states_scale]) if hidden_states_scale is not None else None,
-                ptr_array([x.data_ptr() for x in topk_ids]),
-                ptr_array([x.data_ptr() for x in topk_weights]) if topk_weights is not None else None)
-        addr = lambda a: ctypes.cast(a, ctypes.c_void_p).value if a is not None else None
-        args = _lib.EpDispatchArgsC(addr(keep[0]), addr(keep[1]), addr(keep[2]), addr(keep[3]),
-                                    ctypes.cast(c_counts, ctypes.c_void_p).value, rt,
-                                    _mask_value(active_rank_mask), addr(eplb_ptrs), eplb_bytes,
+        args = _lib.EpDispatchArgsC(_data(hp), _data(sp), _data(ip), _data(wp), _data(c_counts), rt,
+                                    _mask_value(active_rank_mask), _data(eplb_ptrs), eplb_bytes,
                                     dev_counts_ptr)
         with torch.cuda.device(self.device):
             st = self._L.ep_dispatch_ex(self._h, ctypes.byref(args),
                                         ctypes.c_void_p(_stream_ptr(self.device)), ctypes.byref(res))
         if st == _lib.EP_ERR_DEVICE_CHECK:  # checked build: the dispatch happened; keep its state
-            self._counts, self._T = counts, res.tokens_per_rank
+            self._counts, self._T, self._stacked = counts, res.tokens_per_rank, stacked
         check(st)
         T = res.tokens_per_rank
         self._counts, self._T = counts, T
+        self._stacked = stacked
         hs = self._rank_views("hidden", res.recv_hidden, T, H, self.dtype)
         ids = self._rank_views("ids", res.recv_topk_ids, T, K, torch.int32)
         sc = self._rank_views("scale", res.recv_scale, T, G, torch.float32) if res.recv_scale else None
@@ -278,23 +335,35 @@ class EpComm:
         return out if rank is None else out[0]
 
     # -- MoEEpCommunication.combine -----------------------------------------
-    def combine(self, expert_output: Optional[Sequence[Optional[torch.Tensor]]] = None, *,
-                output: Optional[Sequence[torch.Tensor]] = None,
-                active_rank_mask=None) -> List[torch.Tensor]:
+    def combine(self, expert_output=None, *, output=None, active_rank_mask=None):
         """Per source rank, [n_s, hidden] of the combine dtype: the sum over
         the ranks each token was routed to (ascending, fp32, one rounding) of
         their expert_output rows.
 
         ``expert_output[d]`` is rank d's [ep_size*tokens_per_rank, hidden] (or
         [ep_size, tokens_per_rank, hidden]) tensor of the combine dtype; None,
-        or a None entry, means the backend combine input buffer (no copy)."""
+        or a None entry, means the backend combine input buffer (no copy).
+        It may also be one stacked tensor of all ranks' rows,
+        [ep_size, ep_size*tokens_per_rank, hidden]. ``output`` may be a list
+        of [n_s, hidden] tensors or one stacked [ep_size, M, hidden] tensor
+        with M >= every n_s; after a stacked dispatch the default output is
+        one such tensor. The result is the list of per-rank [n_s, hidden]
+        tensors, or the stacked output itself (rank s's result in its first
+        n_s rows; the rows past them are not written)."""
         self._live()
         ep, H = self.ep_size, self.hidden
         if self._counts is None:
             raise EpError(_lib.EP_ERR_STATE, "combine called without a pending dispatch")
         rows = ep * self._T
         eo_ptrs = None
-        if expert_output is not None:
+        if isinstance(expert_output, torch.Tensor):
+            e = expert_output
+            if e.dtype is not self.combine_dtype or not e.is_cuda or e.get_device() != self._dev_index \
+                    or not e.is_contiguous() or e.shape[0] != ep or e.numel() != ep * rows * H or e.shape[-1] != H:
+                raise ValueError(f"a stacked expert_output must be a contiguous {self.combine_dtype} "
+                                 f"[{ep}, {rows}, {H}] tensor on {self.device}")
+            eo_ptrs = self._stacked_ptrs(e, rows, H)
+        elif expert_output is not None:
             if len(expert_output) != ep:
                 raise ValueError(f"expert_output needs {ep} per-rank tensors")
             eo_ptrs = []
@@ -307,23 +376,35 @@ class EpComm:
                     raise ValueError(f"expert_output[{d}] must be contiguous {self.combine_dtype} "
                                      f"[{rows}, {H}] on {self.device}")
                 eo_ptrs.append(e.data_ptr())
-        if output is None:
-            output = [torch.empty(n, H, dtype=self.combine_dtype, device=self.device) for n in self._counts]
+            eo_ptrs = _addr_array(eo_ptrs)
+        if output is None and self._stacked:
+            output = torch.empty(ep, max(self._counts, default=0), H, dtype=self.combine_dtype,
+                                 device=self.device)
+        if isinstance(output, torch.Tensor):
+            o = output
+            if o.dim() != 3 or o.shape[0] != ep or o.shape[2] != H or o.shape[1] < max(self._counts, default=0) \
+                    or o.dtype is not self.combine_dtype or not o.is_cuda or o.get_device() != self._dev_index \
+                    or not o.is_contiguous():
+                raise ValueError(f"a stacked output must be a contiguous {self.combine_dtype} [{ep}, M, {H}] "
+                                 f"tensor on {self.device} with M >= {max(self._counts, default=0)}")
+            out_ptrs = self._stacked_ptrs(o, int(o.shape[1]), H)
         else:
-            if len(output) != ep:
-                raise ValueError(f"output needs {ep} per-rank tensors")
-            for s in range(ep):
-                self._check_rank_tensor("output", output[s], s, self._counts[s], H, self.combine_dtype)
+            if output is None:
+                output = [torch.empty(n, H, dtype=self.combine_dtype, device=self.device) for n in self._counts]
+            else:
+                if len(output) != ep:
+                    raise ValueError(f"output needs {ep} per-rank tensors")
+                for s in range(ep):
+                    self._check_rank_tensor("output", output[s], s, self._counts[s], H, self.combine_dtype)
+            out_ptrs = _addr_array([o.data_ptr() for o in output])
         with torch.cuda.device(self.device):
-            st = self._L.ep_combine(self._h, ptr_array(eo_ptrs) if eo_ptrs is not None else None,
-                                    ptr_array([o.data_ptr() for o in output]),
-                                    _mask_value(active_rank_mask),
+            st = self._L.ep_combine(self._h, _data(eo_ptrs), _data(out_ptrs), _mask_value(active_rank_mask),
                                     ctypes.c_void_p(_stream_ptr(self.device)))
         if st == _lib.EP_ERR_DEVICE_CHECK:  # checked build: the combine happened
             self._counts = None
         check(st)
         self._counts = None
-        return list(output)
+        return output if isinstance(output, torch.Tensor) else list(output)
 
     # -- MoEEpCommunication.destroy -----------------------------------------
     def destroy(self) -> None:
