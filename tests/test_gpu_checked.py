@@ -3,10 +3,11 @@ access of the kernels is tested against the extent of its buffer; an access
 outside is skipped and the call returns EP_ERR_DEVICE_CHECK.
 
 test_gpu_suite_under_checked_build runs the parity, golden, eplb, fuzz,
-graph, stream, device-count, stacked-form and no-alloc GPU tests in a child process that loads the
+graph, stream, device-count, stacked-form, full-size and no-alloc GPU tests in a child process that loads the
 checked library. Every call there waits for its kernels and reads the check
 record, so the suite passing shows that none of those runs touched memory
-outside the buffers the C ABI gives each operand.
+outside the buffers the C ABI gives each operand; the full-size workloads
+include the 32-byte combine path that only combines of 192 MiB or more take.
 
 The child also runs the two tests below, which show that the checks fire.
 They use the checked build's test hook, which declares one access site's
@@ -32,7 +33,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SUITE = ["tests/test_gpu_parity.py", "tests/test_gpu_golden.py", "tests/test_gpu_eplb.py",
          "tests/test_gpu_fuzz.py", "tests/test_gpu_graph.py", "tests/test_gpu_streams.py",
          "tests/test_gpu_checked.py", "tests/test_gpu_device_counts.py", "tests/test_gpu_stacked.py",
-         "tests/test_zz_no_alloc.py"]
+         "tests/test_gpu_fullsize.py", "tests/test_zz_no_alloc.py"]
 
 in_checked_child = pytest.mark.skipif(not _lib.checked(), reason="runs in the checked build's child process")
 
@@ -51,7 +52,7 @@ def test_gpu_suite_under_checked_build(cuda_device):
                        timeout=1800)
     assert r.returncode == 0, r.stdout[-6000:] + r.stderr[-3000:]
     tail = r.stdout.strip().splitlines()[-1]
-    # about a hundred tests pass; the only one the child skips is this one
+    # well over a hundred tests pass; the only one the child skips is this one
     passed = re.search(r"(\d+) passed", tail)
     assert passed and int(passed.group(1)) >= 100 and re.search(r"\b1 skipped\b", tail), tail
 
