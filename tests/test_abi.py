@@ -221,3 +221,20 @@ def test_checked_build_loads_and_exports_the_abi():
 
 def test_normal_build_has_no_test_hook():
     assert not hasattr(_lib.load(), "ep_checked_trim_extent") or _lib.checked()
+
+
+def test_binding_pointer_arrays():
+    """The binding's host arrays of per-rank device pointers: uint64 words, 0 for
+    NULL, and for a stacked [ep, M, cols] tensor base + s * M*cols*element_size."""
+    import numpy as np
+    import torch
+
+    from combine_topk_ids_dest_gb300 import ep as epmod
+    a = epmod._addr_array([0x1000, None, 0, 0x7FFF_FFFF_F000])
+    assert a.dtype == np.uint64 and a.tolist() == [0x1000, 0, 0, 0x7FFF_FFFF_F000]
+    assert epmod._data(None) is None and epmod._data(a) == a.ctypes.data
+    t = torch.zeros(3, 5, 7, dtype=torch.float32)
+    p = epmod.EpComm._stacked_ptrs(t, 5, 7)
+    assert p.dtype == np.uint64
+    assert p.tolist() == [t[s].data_ptr() for s in range(3)]
+    assert epmod.EpComm._stacked_ptrs(t, 5, 7)[2] == t.data_ptr() + 2 * 5 * 7 * 4
