@@ -147,7 +147,15 @@ def test_f16_rne_matches_torch_on_random_tie_and_subnormal_patterns():
     f = allp.view(np.float32)
     ref = torch.from_numpy(f.copy()).to(torch.float16).view(torch.int16).numpy().view(np.uint16)
     for i in range(len(allp)):
-        if np.isnan(f[i]):
-            assert (oracle.f32_bits_to_f16(int(allp[i])) & 0x7C00) == 0x7C00
+        if np.isnan(f[i]):  # a NaN stays a NaN (exponent all ones, mantissa non-zero)
+            r = oracle.f32_bits_to_f16(int(allp[i]))
+            assert (r & 0x7C00) == 0x7C00 and (r & 0x3FF) != 0, hex(int(allp[i]))
             continue
         assert oracle.f32_bits_to_f16(int(allp[i])) == int(ref[i]), hex(int(allp[i]))
+
+
+def test_f16_nan_stays_nan_with_its_sign():
+    for b in (0x7FC00000, 0x7F800001, 0xFFC12345, 0x7FFFFFFF, 0xFF800001):
+        r = oracle.f32_bits_to_f16(b)
+        assert (r & 0x7C00) == 0x7C00 and (r & 0x3FF) != 0, hex(b)
+        assert (r >> 15) == (b >> 31)

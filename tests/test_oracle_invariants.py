@@ -34,9 +34,13 @@ def _run_dispatch(inp, payload=True):
                            active_rank_mask=inp.active_rank_mask, payload=payload)
 
 
-@pytest.mark.parametrize("name", CASES + ["with_invalid", "dups"])
+@pytest.mark.parametrize("name", CASES + ["with_invalid", "dups", "one_scale_column", "three_scale_columns_fp8"])
 def test_dispatch_rows(name):
-    if name == "with_invalid":
+    if name == "one_scale_column":  # scale rows of width 1 travel like any other
+        wl = small(workloads.WORKLOADS["qwen3_mask"]).replace(scales=True, scale_cols_override=1)
+    elif name == "three_scale_columns_fp8":
+        wl = small(workloads.WORKLOADS["dsv3_decode"]).replace(scale_cols_override=3, ep_size=8, num_experts=16)
+    elif name == "with_invalid":
         wl = small(workloads.WORKLOADS["qwen3_mask"]).replace(ids="with_invalid")
     elif name == "dups":
         wl = small(workloads.WORKLOADS["dsv3_decode"]).replace(ids="uniform_dups", ep_size=8,

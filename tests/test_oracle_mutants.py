@@ -54,6 +54,11 @@ MUTANTS = [
     ("hidden_previous_row", "recv_hidden[d][r * row_bytes + b] = hidden[s][(long)t * row_bytes + b];",
      "recv_hidden[d][r * row_bytes + b] = hidden[s][(long)(t > 0 ? t - 1 : 0) * row_bytes + b];"),
     ("identity_scale_group_interleaved", "int group = h / (hidden / scale_cols);", "int group = h % scale_cols;"),
+    ("scale_rows_need_two_columns", "if (scale_cols > 0 && scale && recv_scale && recv_scale[d])",
+     "if (scale_cols > 1 && scale && recv_scale && recv_scale[d])"),
+    ("e4m3_negative_nan_is_a_number", "if (e == 0xF && m == 0x7) {", "if (e == 0xF && m == 0x7 && sign == 0) {"),
+    ("f16_nan_becomes_inf", "return (uint16_t)(sign | (man ? 0x7E00u : 0x7C00u));", "return (uint16_t)(sign | 0x7C00u);"),
+    ("eplb_last_byte_dropped", "for (int b = 0; b < bytes; ++b)\n            global", "for (int b = 0; b + 1 < bytes; ++b)\n            global"),
     ("weights_not_copied", "recv_weights[d][r * top_k + k] = topk_weights[s][(long)t * top_k + k];",
      "recv_weights[d][r * top_k + k] = 0.0f;"),
     ("combine_descending", "                for (int d = 0; d < ep_size; ++d) {\n" + COMBINE_ADD,
