@@ -59,6 +59,35 @@ MUTANTS = [
     ("e4m3_negative_nan_is_a_number", "if (e == 0xF && m == 0x7) {", "if (e == 0xF && m == 0x7 && sign == 0) {"),
     ("f16_nan_becomes_inf", "return (uint16_t)(sign | (man ? 0x7E00u : 0x7C00u));", "return (uint16_t)(sign | 0x7C00u);"),
     ("eplb_last_byte_dropped", "for (int b = 0; b < bytes; ++b)\n            global", "for (int b = 0; b + 1 < bytes; ++b)\n            global"),
+    ("combine_skips_last_token", """    for (int s = 0; s < ep_size; ++s) {
+        for (int t = 0; t < num_tokens[s]; ++t) {
+            long r = (long)s * T + t;
+            const int32_t *ids = topk_ids[s] + (long)t * top_k;
+            for (int h = 0; h < hidden; ++h) {
+                float acc = 0.0f;
+                for (int d = 0; d < ep_size; ++d) {
+""" + COMBINE_ADD, """    for (int s = 0; s < ep_size; ++s) {
+        for (int t = 0; t + 1 < num_tokens[s]; ++t) {
+            long r = (long)s * T + t;
+            const int32_t *ids = topk_ids[s] + (long)t * top_k;
+            for (int h = 0; h < hidden; ++h) {
+                float acc = 0.0f;
+                for (int d = 0; d < ep_size; ++d) {
+""" + COMBINE_ADD),
+    ("combine_skips_last_column", """            for (int h = 0; h < hidden; ++h) {
+                float acc = 0.0f;
+                for (int d = 0; d < ep_size; ++d) {
+""" + COMBINE_ADD, """            for (int h = 0; h + 1 < hidden; ++h) {
+                float acc = 0.0f;
+                for (int d = 0; d < ep_size; ++d) {
+""" + COMBINE_ADD),
+    ("last_id_not_copied", """                for (int k = 0; k < top_k; ++k)
+                    id_row[k] = topk_ids[s][(long)t * top_k + k];""", """                for (int k = 0; k + 1 < top_k; ++k)
+                    id_row[k] = topk_ids[s][(long)t * top_k + k];"""),
+    ("eplb_transposed", "global[(long)r * bytes + b] = local[r][b];", "global[(long)b * ep_size + r] = local[r][b];"),
+    ("weights_reversed", "recv_weights[d][r * top_k + k] = topk_weights[s][(long)t * top_k + k];",
+     "recv_weights[d][r * top_k + k] = topk_weights[s][(long)t * top_k + (top_k - 1 - k)];"),
+    ("bf16_nan_sign_dropped", "return (uint16_t)(((u >> 16) & 0x8000u) | 0x7FC0u);", "return (uint16_t)0x7FC0u;"),
     ("weights_not_copied", "recv_weights[d][r * top_k + k] = topk_weights[s][(long)t * top_k + k];",
      "recv_weights[d][r * top_k + k] = 0.0f;"),
     ("combine_descending", "                for (int d = 0; d < ep_size; ++d) {\n" + COMBINE_ADD,
