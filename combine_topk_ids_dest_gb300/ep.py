@@ -427,3 +427,39 @@ class EpComm:
                 self._h = None
         except Exception:
             pass
+
+
+def combine_noalloc(num_experts: int, top_k: int, topk_ids: Sequence[torch.Tensor],
+                    expert_output: Sequence[torch.Tensor], output: Sequence[torch.Tensor], *,
+                    tokens_per_rank: int, active_rank_mask=None) -> List[torch.Tensor]:
+    """The combine without a communicator and without any device allocation
+    (C ABI ep_combine_noalloc): for callers that may not allocate where they
+    combine. ``topk_ids[s]`` int32 [n_s, top_k] are the ids the dispatch
+    routed; ``expert_output[d]`` bf16 [ep_size*tokens_per_rank, hidden];
+    ``output[s]`` bf16 [n_s, hidden], written in place and returned. The
+    result equals EpComm.combine after EpComm.dispatch of the same ids and
+    mask. Runs on torch's current stream of the tensors' device."""
+    L = _lib.load()
+    ep = len(topk_ids)
+    if len(expert_output) != ep or len(output) != ep:
+        raise ValueError("topk_ids, expert_output and output need one tensor per rank")
+    counts = [int(x.shape[0]) for x in topk_ids]
+    hidden = int(output[0].shape[-1]) if ep else 0
+    dev = expert_output[0].device
+    for name, lst, dtype, cols in (("topk_ids", topk_ids, torch.int32, top_k), ("output", output, torch.bfloat16, hidden)):
+        for s, t in enumerate(lst):
+            if t.dtype is not dtype or t.device != dev or not t.is_contiguous() or t.dim() != 2 or t.shape != (counts[s], cols):
+                raise ValueError(f"{name}[{s}] must be a contiguous {dtype} [{counts[s]}, {cols}] tensor on {dev}")
+    rows = ep * int(tokens_per_rank)
+    for d, e in enumerate(expert_output):
+        if e.dtype is not torch.bfloat16 or e.device != dev or not e.is_contiguous() or e.numel() != rows * hidden:
+            raise ValueError(f"expert_output[{d}] must be a contiguous bf16 [{rows}, {hidden}] tensor on {dev}")
+    ids = _addr_array([x.data_ptr() for x in topk_ids])
+    eo = _addr_array([x.data_ptr() for x in expert_output])
+    out = _addr_array([x.data_ptr() for x in output])
+    c_counts = np.array(counts, dtype=np.int32)
+    with torch.cuda.device(dev):
+        check(L.ep_combine_noalloc(ep, int(num_experts), int(top_k), hidden, int(tokens_per_rank),
+                                   _data(c_counts), _data(ids), _mask_value(active_rank_mask), _data(eo), _data(out),
+                                   ctypes.c_void_p(_stream_ptr(dev))))
+    return list(output)

@@ -81,3 +81,31 @@ def test_noalloc_rejects_sizes_beyond_its_scratch():
     st = L.ep_combine_noalloc(ep, 64, 8, 256, T, counts, nulls, _lib.ALL_RANKS, nulls, nulls, None)
     assert st == EP_ERR_INVALID_ARG
     assert b"static scratch" in L.ep_last_error()
+
+
+@pytest.mark.gpu
+def test_python_wrapper_matches_combine(cuda_device):
+    from combine_topk_ids_dest_gb300 import combine_noalloc
+    wl = ROUNDS[0]
+    inp = workloads.make_inputs(wl)
+    comm = EpComm(wl.ep_size, wl.num_experts, wl.top_k, wl.hidden, wl.capacity, enable_rank_mask=True,
+                  device=cuda_device)
+    try:
+        ids = to_dev(inp.topk_ids, cuda_device)
+        mask = inp.active_rank_mask
+        res = comm.dispatch(to_dev(inp.hidden, cuda_device), ids, to_dev(inp.topk_weights, cuda_device),
+                            runtime_max_tokens_per_rank=wl.runtime_max, active_rank_mask=mask)
+        eo = fill_expert_outputs(comm, res.tokens_per_rank, cuda_device, caller=True)
+        want = comm.combine(eo, active_rank_mask=mask)
+        got = [torch.full((n, wl.hidden), float("nan"), dtype=torch.bfloat16, device=cuda_device)
+               for n in inp.num_tokens]
+        ret = combine_noalloc(wl.num_experts, wl.top_k, ids, eo, got, tokens_per_rank=res.tokens_per_rank,
+                              active_rank_mask=mask)
+        torch.cuda.synchronize(cuda_device)
+        assert all(r is g for r, g in zip(ret, got))
+        for s in range(wl.ep_size):
+            np.testing.assert_array_equal(_bits(got[s]), _bits(want[s]), err_msg=f"output of rank {s}")
+        with pytest.raises(ValueError):
+            combine_noalloc(wl.num_experts, wl.top_k, ids, eo, got[:-1], tokens_per_rank=res.tokens_per_rank)
+    finally:
+        comm.destroy()
