@@ -781,6 +781,9 @@ def main():
             counts=counts)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
+    if args.gpus != world and rank == 0:
+        print(f"bench.py: --gpus {args.gpus} but {world} process(es) were launched; measuring {world} "
+              "(start N>1 with torch.distributed.run, one process per GPU)", file=sys.stderr)
     if args.impl == "reference":
         run_reference(args, rank, world)
         return
