@@ -117,8 +117,9 @@ typedef struct {
     int ep_size;               /* 1..64 ranks */
     int num_experts;           /* a positive multiple of ep_size */
     int top_k;                 /* 1..32 */
-    int hidden;                /* payload columns; hidden*elem_bytes a multiple of 16,
-                                  hidden % 8 == 0, hidden <= 2^28 */
+    int hidden;                /* payload columns, <= 2^28; hidden*elem_bytes a multiple of 16
+                                  for the payload and for the combine dtype (so hidden % 8 == 0
+                                  for a bf16 or fp16 combine, hidden % 4 == 0 for fp32) */
     int max_tokens_per_rank;   /* capacity C >= 0 */
     ep_dtype dtype;            /* payload type of the hidden rows */
     int enable_rank_mask;      /* 0/1 */
