@@ -34,9 +34,12 @@ def _run_dispatch(inp, payload=True):
                            active_rank_mask=inp.active_rank_mask, payload=payload)
 
 
-@pytest.mark.parametrize("name", CASES + ["with_invalid", "dups", "one_scale_column", "three_scale_columns_fp8"])
+@pytest.mark.parametrize("name", CASES + ["with_invalid", "dups", "one_scale_column", "three_scale_columns_fp8",
+                                  "mask_on_high_ranks"])
 def test_dispatch_rows(name):
-    if name == "one_scale_column":  # scale rows of width 1 travel like any other
+    if name == "mask_on_high_ranks":  # the mask is 64 bits: ranks 32..63 are masked like the others
+        wl = small(workloads.WORKLOADS["dsv3_decode"]).replace(dropped_ranks=(0, 31, 32, 40, 63))
+    elif name == "one_scale_column":  # scale rows of width 1 travel like any other
         wl = small(workloads.WORKLOADS["qwen3_mask"]).replace(scales=True, scale_cols_override=1)
     elif name == "three_scale_columns_fp8":
         wl = small(workloads.WORKLOADS["dsv3_decode"]).replace(scale_cols_override=3, ep_size=8, num_experts=16)

@@ -88,6 +88,18 @@ MUTANTS = [
     ("weights_reversed", "recv_weights[d][r * top_k + k] = topk_weights[s][(long)t * top_k + k];",
      "recv_weights[d][r * top_k + k] = topk_weights[s][(long)t * top_k + (top_k - 1 - k)];"),
     ("bf16_nan_sign_dropped", "return (uint16_t)(((u >> 16) & 0x8000u) | 0x7FC0u);", "return (uint16_t)0x7FC0u;"),
+    ("mask_read_as_32_bits", "if (mask_enabled && !((active_rank_mask >> d) & 1u))",
+     "if (mask_enabled && !(((uint32_t)active_rank_mask >> (d & 31)) & 1u))"),
+    ("e4m3_sign_dropped", "    return sign ? -mag : mag;\n}\n\n/* IEEE 754 binary16", "    return mag;\n}\n\n/* IEEE 754 binary16"),
+    ("f16_carry_lost", "uint32_t field = ((uint32_t)base_exp << 10) + (keep - 0x400u);",
+     "uint32_t field = ((uint32_t)base_exp << 10) | (keep & 0x3FFu);"),
+    ("identity_fp8_scale_ignored", """                    x = oracle_e4m3_to_f32(recv_hidden[d][r * hidden + h]) *
+                        recv_scale[d][r * scale_cols + group];""", """                    x = oracle_e4m3_to_f32(recv_hidden[d][r * hidden + h]) *
+                        (group >= 0 ? 1.0f : recv_scale[d][r * scale_cols + group]);"""),
+    ("eplb_all_rows_from_rank0", "global[(long)r * bytes + b] = local[r][b];", "global[(long)r * bytes + b] = local[0][b];"),
+    ("invalid_row_last_id_stale", """                    for (int k = 0; k < top_k; ++k)
+                        id_row[k] = ORACLE_INVALID_EXPERT_ID;""", """                    for (int k = 0; k + 1 < top_k; ++k)
+                        id_row[k] = ORACLE_INVALID_EXPERT_ID;"""),
     ("weights_not_copied", "recv_weights[d][r * top_k + k] = topk_weights[s][(long)t * top_k + k];",
      "recv_weights[d][r * top_k + k] = 0.0f;"),
     ("combine_descending", "                for (int d = 0; d < ep_size; ++d) {\n" + COMBINE_ADD,
