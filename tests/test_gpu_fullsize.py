@@ -48,10 +48,16 @@ LARGE = {
         combine_dtype=cdt, dropped_ranks=(2,), seed=31)
     for cdt in ("bf16", "fp16", "fp32")
 }
+# One receive region (and one combine-input region) larger than 4 GiB: 64 KB fp32
+# rows, 4 ranks x 16400 slots; only rank 3 sends, so its last slots lie more than
+# 2^32 bytes into every region while the inputs stay at about 1 GB.
+LARGE["region_over_4gib"] = workloads.EpWorkload(
+    name="region_over_4gib", ep_size=4, num_experts=8, top_k=2, hidden=16384, dtype="fp32", capacity=16400,
+    runtime_max=None, counts=("fixed", 0, 0, 0, 16400), combine_dtype="fp32", seed=33)
 
 
 @pytest.mark.parametrize("name", ["mixtral_decode", "dsv3_decode", "dsv3_prefill", "qwen3_mask",
-                                  "large_bf16", "large_fp16", "large_fp32"])
+                                  "large_bf16", "large_fp16", "large_fp32", "region_over_4gib"])
 def test_full_size_sampled(cuda_device, name):
     from combine_topk_ids_dest_gb300 import EpComm
     wl = workloads.WORKLOADS[name] if name in workloads.WORKLOADS else LARGE[name]
