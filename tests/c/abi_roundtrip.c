@@ -6,7 +6,9 @@
  * ep_size 2, 4 experts (0,1 on rank 0; 2,3 on rank 1), top_k 2, hidden 8
  * bf16, 3 tokens per rank. Rank 0 sends ids {0,1} and {1,3}; rank 1 sends
  * {2,3}. Checks every receive id row, the routed hidden rows, and three
- * combine outputs worked by hand. Exit status 0 on success.
+ * combine outputs worked by hand; then a second round through
+ * ep_dispatch_ex with device-side token counts (rank 0 sends only its first
+ * token). Exit status 0 on success.
  */
 #include <stdint.h>
 #include <stdio.h>
@@ -126,6 +128,52 @@ int main(void)
         expect(o1[0][c] == 0x3FC0, "token (1,0) = 1.5");
     }
     expect(ep_combine(h, NULL, out, UINT64_MAX, NULL) == EP_ERR_STATE, "second combine is refused");
+
+    /* A second round through ep_dispatch_ex with device-side token counts:
+     * rank 0 may send 2 tokens (its host count is the maximum) but sends 1. */
+    const int32_t dcounts[EP] = {1, 1};
+    void *d_counts;
+    if (cudaMalloc(&d_counts, 16)) {
+        fprintf(stderr, "cudaMalloc failed\n");
+        return 2;
+    }
+    cudaMemcpy(d_counts, dcounts, sizeof dcounts, cudaMemcpyHostToDevice);
+    ep_dispatch_args args;
+    memset(&args, 0, sizeof args);
+    args.hidden = hidden;
+    args.topk_ids = ids;
+    args.num_tokens = counts;
+    args.runtime_max_tokens_per_rank = -1;
+    args.active_rank_mask = UINT64_MAX;
+    args.num_tokens_device = (const int32_t *)((const char *)d_counts + 2);
+    expect(ep_dispatch_ex(h, &args, NULL, &res) == EP_ERR_INVALID_ARG, "misaligned device counts are refused");
+    args.num_tokens_device = (const int32_t *)d_counts;
+    if (!ok(ep_dispatch_ex(h, &args, NULL, &res), "ep_dispatch_ex with device counts"))
+        return 1;
+    const int32_t want2[EP][EP * T][2] = {
+        {{0, 1}, {-1, -1}, {-1, -1}, {-1, -1}, {-1, -1}, {-1, -1}},
+        {{-1, -1}, {-1, -1}, {-1, -1}, {2, 3}, {-1, -1}, {-1, -1}},
+    };
+    for (int d = 0; d < EP; ++d) {
+        int32_t got[EP * T][2];
+        cudaMemcpy(got, res.recv_topk_ids[d], sizeof got, cudaMemcpyDeviceToHost);
+        expect(memcmp(got, want2[d], sizeof got) == 0, "id planes follow the device counts");
+    }
+    uint16_t sentinel[2][H];
+    for (int i = 0; i < 2 * H; ++i)
+        sentinel[i / H][i % H] = 0x7FC1;
+    cudaMemcpy(d_o0, sentinel, sizeof sentinel, cudaMemcpyHostToDevice);
+    /* the combine-input buffers still hold the expert outputs written above */
+    if (!ok(ep_combine(h, NULL, out, UINT64_MAX, NULL), "ep_combine after device counts"))
+        return 1;
+    cudaMemcpy(o0, d_o0, sizeof o0, cudaMemcpyDeviceToHost);
+    cudaMemcpy(o1, d_o1, sizeof o1, cudaMemcpyDeviceToHost);
+    for (int c = 0; c < H; ++c) {
+        expect(o0[0][c] == 0x4000, "device counts: token (0,0) = 2.0");
+        expect(o0[1][c] == 0x7FC1, "device counts: the row past rank 0's count is left alone");
+        expect(o1[0][c] == 0x3FC0, "device counts: token (1,0) = 1.5");
+    }
+    cudaFree(d_counts);
     if (!ok(ep_destroy(h), "ep_destroy"))
         return 1;
     if (failures)
