@@ -153,9 +153,14 @@ class EpComm:
         if self._h is None:
             raise EpError(_lib.EP_ERR_STATE, "the communicator was destroyed")
 
-    def _check_rank_tensor(self, name, t, s, n, cols, dtype):
+    def _check_rank_tensor(self, name, t, s, n, cols, dtype, rows_any_shape=False):
+        """A per-rank operand: contiguous [n, cols] of `dtype` on the device. With
+        rows_any_shape, [n, *] whose trailing dimensions hold `cols` elements per
+        row (the pages give hidden_states and its scales as [local_num_tokens, *])."""
         if t.dtype is not dtype or not t.is_cuda or t.get_device() != self._dev_index:
             raise ValueError(f"{name}[{s}] is {t.dtype} on {t.device}, expected {dtype} on {self.device}")
+        if rows_any_shape and t.dim() >= 2 and t.shape[0] == n and t.numel() == n * cols and t.is_contiguous():
+            return
         if t.shape != (n, cols) or not t.is_contiguous():
             raise ValueError(f"{name}[{s}] must be a contiguous [{n}, {cols}] tensor, got "
                              f"{tuple(t.shape)}")
@@ -202,6 +207,8 @@ class EpComm:
         communicator), ``topk_ids[s]`` int32 [n_s, top_k], optional
         ``topk_weights[s]`` fp32 [n_s, top_k] and ``hidden_states_scale[s]``
         fp32 [n_s, scale_cols]. Weights and scales are all-or-none over ranks.
+        Hidden rows and scale rows may also come as [n_s, *] with that many
+        elements per row (e.g. [n_s, heads, head_dim]).
         ``eplb_local_stats[s]`` (optional, every rank the same dtype and shape,
         a multiple of 4 bytes) is gathered into ``eplb_global_stats``.
 
@@ -251,13 +258,13 @@ class EpComm:
             counts = [int(x.shape[0]) for x in hidden_states]
             for s in range(ep):
                 n = counts[s]
-                self._check_rank_tensor("hidden_states", hidden_states[s], s, n, H, self.dtype)
+                self._check_rank_tensor("hidden_states", hidden_states[s], s, n, H, self.dtype, True)
                 self._check_rank_tensor("topk_ids", topk_ids[s], s, n, K, torch.int32)
                 if topk_weights is not None:
                     self._check_rank_tensor("topk_weights", topk_weights[s], s, n, K, torch.float32)
                 if hidden_states_scale is not None:
                     self._check_rank_tensor("hidden_states_scale", hidden_states_scale[s], s, n, G,
-                                            torch.float32)
+                                            torch.float32, True)
             hp = _addr_array([x.data_ptr() for x in hidden_states])
             ip = _addr_array([x.data_ptr() for x in topk_ids])
             wp = _addr_array([x.data_ptr() for x in topk_weights]) if topk_weights is not None else None

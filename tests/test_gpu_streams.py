@@ -115,6 +115,35 @@ def test_handles_used_from_two_host_threads(cuda_device):
             np.testing.assert_array_equal(bf16_bits(outs[s]), out[s])
 
 
+def test_hidden_rows_of_any_trailing_shape(cuda_device):
+    """hidden_states[s] as [n, 4, H/4] (the pages' [local_num_tokens, *]) gives
+    exactly what [n, H] gives; a wrong element count per row is refused."""
+    wl = workloads.EpWorkload(name="shape", ep_size=4, num_experts=8, top_k=2, hidden=256, dtype="bf16",
+                              capacity=16, runtime_max=None, counts=("uniform", 0, 16), seed=76)
+    inp = workloads.make_inputs(wl)
+    comms = [EpComm(wl.ep_size, wl.num_experts, wl.top_k, wl.hidden, wl.capacity, device=cuda_device)
+             for _ in range(2)]
+    try:
+        h2 = to_dev(inp.hidden, cuda_device)
+        h3 = [x.view(x.shape[0], 4, wl.hidden // 4) for x in h2]
+        ids = to_dev(inp.topk_ids, cuda_device)
+        a = comms[0].dispatch(h3, ids)
+        b = comms[1].dispatch(h2, ids)
+        torch.cuda.synchronize(cuda_device)
+        for d in range(wl.ep_size):
+            assert torch.equal(a.topk_ids[d], b.topk_ids[d])
+            valid = (b.topk_ids[d] != INV).any(dim=1)
+            assert torch.equal(a.hidden_states[d][valid].view(torch.int16), b.hidden_states[d][valid].view(torch.int16))
+        for c in comms:
+            c.combine()
+        bad = [x.view(x.shape[0], 4, wl.hidden // 4)[:, :3] for x in h2]  # 3/4 of each row
+        with pytest.raises(ValueError):
+            comms[0].dispatch(bad, ids)
+    finally:
+        for c in comms:
+            c.destroy()
+
+
 def test_binding_rejects_wrong_tensors(cuda_device):
     comm = EpComm(2, 4, 2, 64, 8, device=cuda_device)
     try:
