@@ -122,3 +122,40 @@ def test_stacked_argument_checks(cuda_device):
         assert out.shape == (2, 5, 64)
     finally:
         comm.destroy()
+
+
+def test_stacked_form_with_device_counts(cuda_device):
+    """Stacked operands with device-side counts: the same as per-rank tensors cut
+    to those counts."""
+    inp = workloads.make_inputs(WL)
+    mask = inp.active_rank_mask
+    M = WL.tokens_per_rank
+    dev_counts = [min(n, 5) if s % 3 else n for s, n in enumerate(inp.num_tokens)]
+    comms = [EpComm(WL.ep_size, WL.num_experts, WL.top_k, WL.hidden, WL.capacity, dtype=WL.torch_dtype,
+                    enable_rank_mask=True, device=cuda_device) for _ in range(2)]
+    try:
+        rows = torch.arange(WL.ep_size * M, device=cuda_device)
+        eo = torch.stack([workloads.expert_output_rows(EO_SEED, d, rows, WL.hidden, device=cuda_device)
+                          for d in range(WL.ep_size)])
+        a = comms[0].dispatch(_stack(inp.hidden, M, 0x7E).to(cuda_device), _stack(inp.topk_ids, M, 0).to(cuda_device),
+                              _stack(inp.topk_weights, M, 0x40).to(cuda_device),
+                              hidden_states_scale=_stack(inp.scale, M, 0x40).to(cuda_device),
+                              runtime_max_tokens_per_rank=WL.runtime_max, active_rank_mask=mask,
+                              num_tokens=inp.num_tokens,
+                              num_tokens_device=torch.tensor(dev_counts, dtype=torch.int32, device=cuda_device))
+        out_a = comms[0].combine(eo, active_rank_mask=mask)
+        cut = lambda lst: [x[:n].contiguous().to(cuda_device) for x, n in zip(lst, dev_counts)]
+        b = comms[1].dispatch(cut(inp.hidden), cut(inp.topk_ids), cut(inp.topk_weights),
+                              hidden_states_scale=cut(inp.scale), runtime_max_tokens_per_rank=WL.runtime_max,
+                              active_rank_mask=mask)
+        out_b = comms[1].combine(eo, active_rank_mask=mask)
+        torch.cuda.synchronize(cuda_device)
+        for d in range(WL.ep_size):
+            assert torch.equal(a.topk_ids[d], b.topk_ids[d]), f"ids of rank {d}"
+            valid = (b.topk_ids[d] != INV).any(dim=1)
+            assert torch.equal(a.hidden_states[d][valid].view(torch.uint8), b.hidden_states[d][valid].view(torch.uint8))
+        for s, n in enumerate(dev_counts):
+            assert torch.equal(out_a[s, :n].view(torch.int16), out_b[s].view(torch.int16)), f"rank {s}"
+    finally:
+        for c in comms:
+            c.destroy()
