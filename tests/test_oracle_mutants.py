@@ -100,6 +100,14 @@ MUTANTS = [
     ("invalid_row_last_id_stale", """                    for (int k = 0; k < top_k; ++k)
                         id_row[k] = ORACLE_INVALID_EXPERT_ID;""", """                    for (int k = 0; k + 1 < top_k; ++k)
                         id_row[k] = ORACLE_INVALID_EXPERT_ID;"""),
+    ("receive_row_without_source_offset", "recv_hidden[d][r * row_bytes + b] = hidden[s][(long)t * row_bytes + b];",
+     "recv_hidden[d][(long)t * row_bytes + b] = hidden[s][(long)t * row_bytes + b];"),
+    ("combine_reads_transposed_rows", "acc = acc + oracle_bf16_to_f32(expert_output[d][r * hidden + h]);",
+     "acc = acc + oracle_bf16_to_f32(expert_output[d][((long)t * ep_size + s) * hidden + h]);"),
+    ("f16_subnormal_shift_off_by_one", "shift = 13 + (-14 - e);  /* subnormal: grid of 2^-24 */",
+     "shift = 14 + (-14 - e);  /* subnormal: grid of 2^-24 */"),
+    ("identity_bf16_bytes_swapped", "x = oracle_bf16_to_f32((uint16_t)(p[0] | (p[1] << 8)));",
+     "x = oracle_bf16_to_f32((uint16_t)((p[0] << 8) | p[1]));"),
     ("weights_not_copied", "recv_weights[d][r * top_k + k] = topk_weights[s][(long)t * top_k + k];",
      "recv_weights[d][r * top_k + k] = 0.0f;"),
     ("combine_descending", "                for (int d = 0; d < ep_size; ++d) {\n" + COMBINE_ADD,
