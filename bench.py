@@ -367,6 +367,15 @@ class ClockSampler:
         return self.summarise(self.parse_smi(lines), "nvidia-smi", self.SMI_PERIOD_MS)
 
 
+def _quantile(xs, q):
+    """q-quantile of xs by linear interpolation between order statistics."""
+    ys = sorted(xs)
+    pos = q * (len(ys) - 1)
+    lo = int(pos)
+    hi = min(lo + 1, len(ys) - 1)
+    return ys[lo] + (ys[hi] - ys[lo]) * (pos - lo)
+
+
 def reduce_max(values, device=None):
     """Element-wise max over all ranks of the default process group (identity
     without one): the slowest replica sets the time of the whole job."""
@@ -601,6 +610,8 @@ def run_ours(args, rank, world):
         "vs_baseline": None, "dtype": "fp32", "data": "synthetic",
         "config": workload_config(wl, b),
         "us_per_round": 1e3 * ms, "us_per_round_median": 1e3 * statistics.median(t_round),
+        "us_per_round_p10_p90_max": [1e3 * _quantile(t_round, 0.1), 1e3 * _quantile(t_round, 0.9),
+                                     1e3 * max(t_round)],
         "pct_hbm_peak": 100.0 * b["total"] / (ms / 1e3) / 1e9 / peak,
         "payload_gbs": b["payload"] / (ms / 1e3) / 1e9,
         "roofline": {"bound": "hbm", "kernel": top, "achieved": per[top]["achieved"], "peak": peak,

@@ -134,3 +134,10 @@ def test_clock_poller_process_reports_unavailable_without_nvml():
     r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--clock-poller", "GPU-none", "0.002"],
                        capture_output=True, text=True, timeout=120)
     assert r.returncode == 0 and r.stdout.startswith("unavailable")
+
+
+def test_quantile():
+    import bench
+    assert bench._quantile([3, 1, 2, 5, 4], 0.5) == 3
+    assert abs(bench._quantile([1, 2, 3, 4, 5], 0.1) - 1.4) < 1e-12
+    assert bench._quantile([7], 0.9) == 7
