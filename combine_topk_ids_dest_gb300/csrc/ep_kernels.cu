@@ -24,9 +24,15 @@
 // as 4 16-byte or, for large aligned combines, 2 32-byte vectors):
 //   reads the row's slot in each routed rank's combine input in ascending
 //   rank order, two ranks' loads in flight before their adds, adds in fp32
-//   from +0.0 and rounds once to bf16 (page "flashinfer.moe_ep.
-//   MoEEpCommunication", combine(): per token, the ranks' expert outputs are
-//   added up).
+//   from +0.0 and rounds once to the combine type (bf16 or fp16; fp32 sums
+//   are stored as they are) (page "flashinfer.moe_ep.MoEEpCommunication",
+//   combine(): per token, the ranks' expert outputs are added up).
+//
+// With device-side token counts the dispatch reads each rank's count when it
+// runs (clamped to the host maximum) and leaves it for the combine, whose
+// blocks past it exit. In the checked build (EP_CHECKED) every global access
+// is tested against its buffer first (EP_IN_BOUNDS); in the normal build
+// those tests compile to nothing.
 //
 // Nothing here is a dense contraction; both kernels are bound by HBM
 // bandwidth, so the design is about coalesced 16- and 32-byte accesses and
