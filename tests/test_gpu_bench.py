@@ -26,9 +26,12 @@ def test_bench_line_on_gpu(cuda_device):
     assert rf["bound"] == "hbm" and rf["unit"] == "GB/s" and rf["peak"] > 0
     assert abs(rf["frac"] - rf["achieved"] / rf["peak"]) < 1e-9
     assert set(rf["kernels"]) == {"dispatch_kernel", "combine_kernel"}
+    assert "traffic" in rf and (rf["traffic"] is None or rf["traffic"] > 0)
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] == 1 and cb["value"] > 0 and cb["sample"]
     e2e = d["e2e"]
     assert e2e["value"] > 0 and e2e["h2d_bytes_per_step"] > 0 and e2e["d2h_bytes_per_step"] > 0
-    assert "sm_mhz" in d["clocks"] and "reasons" in d["clocks"]
+    assert "sm_mhz" in d["clocks"] and "reasons" in d["clocks"] and "source" in d["clocks"]
+    p10, p90, mx = d["us_per_round_p10_p90_max"]
+    assert 0 < p10 <= p90 <= mx
     assert d["config"]["workload"] == "tiny"
