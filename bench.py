@@ -125,6 +125,7 @@ import workloads  # noqa: E402
 
 METRIC = "dispatch+combine µs/round and routed-payload GB/s as % of GB300 HBM peak"
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e nominal bandwidth (7.9 TB/s), for context beside the measured peak
 L2_FLUSH_BYTES = 256 << 20
 # Sources whose code decides what the profiled kernels do: the kernels and
 # their argument blocks.
@@ -472,7 +473,7 @@ def run_reference(args, rank, world):
         "impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / len(times),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp32",
-        "data": "synthetic", "config": workload_config(wl, full),
+        "data": "synthetic", "config": workload_config(wl, full, args.l2_flush),
         "us_per_round_extrapolated": 1e6 * full["total"] / (gbs * 1e9),
         "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": desc,
                          "host_cores_available": len(os.sched_getaffinity(0))},
@@ -481,15 +482,19 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
-def workload_config(wl, b):
+def workload_config(wl, b, l2_flush):
+    """The workload, as both arms print it (same object for the same arguments)."""
+    l2 = {"write": "L2 flushed before each timed step, outside its events: 256 MB written",
+          "write+read": "L2 flushed before each timed step, outside its events: 256 MB written then "
+                        "read back (clean, cold L2)"}[l2_flush]
+    if b["total"] > (128 << 20):
+        l2 += "; per-round traffic larger than L2"
     return {"workload": wl.name, "ep_size": wl.ep_size, "num_experts": wl.num_experts,
             "top_k": wl.top_k, "hidden": wl.hidden,
             "payload": wl.dtype + (f" + fp32 scales [n,{wl.scale_cols}]" if wl.scales else ""),
             "max_tokens_per_rank": wl.capacity, "tokens_per_rank": wl.tokens_per_rank,
             "ids": wl.ids, "rank_mask_drops": list(wl.dropped_ranks) if wl.dropped_ranks else None,
-            "tokens": b["N"], "routed_pairs": b["P"], "bytes_per_round": b["total"],
-            "l2": "L2 flushed before each timed step, outside its events: 256 MB written then read "
-                  "back (clean, cold L2); the prefill inputs are also larger than L2",
+            "tokens": b["N"], "routed_pairs": b["P"], "bytes_per_round": b["total"], "l2": l2,
             "combine_input": "backend buffer, filled once with stand-in expert outputs (untimed)"}
 
 
@@ -608,15 +613,20 @@ def run_ours(args, rank, world):
         "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "fp32", "data": "synthetic",
-        "config": workload_config(wl, b),
+        "config": workload_config(wl, b, args.l2_flush),
         "us_per_round": 1e3 * ms, "us_per_round_median": 1e3 * statistics.median(t_round),
         "us_per_round_p10_p90_max": [1e3 * _quantile(t_round, 0.1), 1e3 * _quantile(t_round, 0.9),
                                      1e3 * max(t_round)],
         "pct_hbm_peak": 100.0 * b["total"] / (ms / 1e3) / 1e9 / peak,
+        "pct_nominal_hbm": 100.0 * b["total"] / (ms / 1e3) / 1e9 / NOMINAL_HBM_GBS,
         "payload_gbs": b["payload"] / (ms / 1e3) / 1e9,
         "roofline": {"bound": "hbm", "kernel": top, "achieved": per[top]["achieved"], "peak": peak,
                      "unit": "GB/s", "frac": per[top]["frac"], "traffic": per[top]["traffic"],
-                     "peak_source": peak_src, "kernels": per},
+                     "peak_source": peak_src,
+                     "peak_kind": "a measured copy bandwidth (equal bytes read and written); a kernel whose "
+                                  "traffic is mostly reads or mostly writes can stream above it",
+                     "nominal_peak": NOMINAL_HBM_GBS, "frac_of_nominal": per[top]["achieved"] / NOMINAL_HBM_GBS,
+                     "kernels": per},
         "e2e": {"value": whole_job_gbs(b["total"], 1, world, e2e_ms), "unit": "GB/s", "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes, "steps": e2e_steps,
                 "path": "pinned host inputs (one packed buffer) -> one H2D copy -> EpComm.dispatch/combine "
@@ -634,12 +644,6 @@ def run_ours(args, rank, world):
         "gpu_launches": launches_per_round * args.steps,
         "clocks": clocks.summary(),
     }
-    l2 = {"write": "L2 flushed before each timed step, outside its events: 256 MB written",
-          "write+read": "L2 flushed before each timed step, outside its events: 256 MB written then "
-                        "read back (clean, cold L2)"}[args.l2_flush]
-    if b["total"] > (128 << 20):
-        l2 += "; per-round traffic larger than L2"
-    line["config"]["l2"] = l2
     if world == 1 and not args.no_cpu_baseline:
         s, eo, sb, desc = oracle_sample(inp, args.cpu_seconds)
         t0 = time.perf_counter()

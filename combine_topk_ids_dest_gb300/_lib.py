@@ -42,7 +42,7 @@ ALL_RANKS = (1 << 64) - 1  # "no mask": every rank active
 EXPORTS = ("ep_is_supported", "ep_workspace_size", "ep_create", "ep_create_with_workspace",
            "ep_dispatch", "ep_get_combine_input_buffer", "ep_combine", "ep_destroy",
            "ep_rank_mask", "ep_last_error", "ep_combine_noalloc", "ep_workspace_size_ex",
-           "ep_create_ex", "ep_dispatch_ex")
+           "ep_create_ex", "ep_dispatch_ex", "ep_binary_version")
 EP_NOALLOC_MAX_SLOTS = 65536
 
 
@@ -136,6 +136,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         L.ep_dispatch_ex.restype = i32
         L.ep_combine_noalloc.argtypes = [i32, i32, i32, i32, i32, P, P, u64, P, P, P]
         L.ep_combine_noalloc.restype = i32
+        L.ep_binary_version.argtypes = [ctypes.POINTER(i32)]
+        L.ep_binary_version.restype = i32
         L.ep_last_error.argtypes = []
         L.ep_last_error.restype = ctypes.c_char_p
         if checked():

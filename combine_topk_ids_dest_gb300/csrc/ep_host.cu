@@ -747,4 +747,24 @@ uint64_t ep_rank_mask(const int *ranks, int n)
 
 const char *ep_last_error(void) { return g_err; }
 
+ep_status ep_binary_version(int *version)
+{
+    if (!version)
+        return fail(EP_ERR_INVALID_ARG, "version is NULL");
+    *version = 0;
+    int v[16], n = 0;
+    cudaError_t ce = epk::kernel_binary_versions(v, 15, &n);
+    if (ce == cudaSuccess && n < 16)
+        ce = epk::noalloc_binary_version(&v[n++]);
+    if (ce != cudaSuccess) {
+        cudaGetLastError();
+        return fail(EP_ERR_CUDA, "cudaFuncGetAttributes: %s", cudaGetErrorString(ce));
+    }
+    for (int i = 1; i < n; ++i)
+        if (v[i] != v[0])
+            return fail(EP_ERR_UNSUPPORTED, "kernel %d reports binary version %d, kernel 0 %d", i, v[i], v[0]);
+    *version = v[0];
+    return ok();
+}
+
 }  // extern "C"

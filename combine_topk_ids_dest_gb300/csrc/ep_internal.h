@@ -133,6 +133,14 @@ struct CombineArgs {
 // EP_OK) and returns `st`.
 ep_status set_error(ep_status st, const char *fmt, ...);
 
+// binaryVersion (compute capability major*10 + minor of the loaded code) of
+// every dispatch and combine kernel instance, as cudaFuncGetAttributes reports
+// it on the current device: up to `max` values into `out`, the number of
+// kernels into *n. The no-alloc routing kernel reports through
+// noalloc_binary_version.
+cudaError_t kernel_binary_versions(int *out, int max, int *n);
+cudaError_t noalloc_binary_version(int *out);
+
 // Queue one launch on `stream`; returns the launch's cudaError_t.
 cudaError_t launch_dispatch(const DispatchArgs &a, cudaStream_t stream);
 cudaError_t launch_combine(const CombineArgs &a, cudaStream_t stream);

@@ -562,6 +562,31 @@ int sm_count()
 
 }  // namespace
 
+cudaError_t kernel_binary_versions(int *out, int max, int *n)
+{
+    const void *fns[] = {
+        reinterpret_cast<const void *>(dispatch_kernel<16>),
+        reinterpret_cast<const void *>(dispatch_kernel<32>),
+        reinterpret_cast<const void *>(combine_kernel<EP_DTYPE_BF16, 16>),
+        reinterpret_cast<const void *>(combine_kernel<EP_DTYPE_BF16, 32>),
+        reinterpret_cast<const void *>(combine_kernel<EP_DTYPE_FP16, 16>),
+        reinterpret_cast<const void *>(combine_kernel<EP_DTYPE_FP16, 32>),
+        reinterpret_cast<const void *>(combine_kernel<EP_DTYPE_FP32, 16>),
+        reinterpret_cast<const void *>(combine_kernel<EP_DTYPE_FP32, 32>),
+    };
+    *n = 0;
+    for (const void *f : fns) {
+        cudaFuncAttributes attr;
+        cudaError_t ce = cudaFuncGetAttributes(&attr, f);
+        if (ce != cudaSuccess)
+            return ce;
+        if (*n < max)
+            out[*n] = attr.binaryVersion;
+        ++*n;
+    }
+    return cudaSuccess;
+}
+
 cudaError_t launch_dispatch(const DispatchArgs &a, cudaStream_t stream)
 {
     const long long n_slots = (long long)a.ep * a.T;

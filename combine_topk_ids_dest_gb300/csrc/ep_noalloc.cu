@@ -3,10 +3,9 @@
 //
 // Some callers of this library may not call cudaMalloc (or any allocator)
 // at the point where they combine: code inside a memory arena that owns all
-// device memory after start-up, plug-ins hosted by an inference runtime that
-// forbids allocations of their own, and code between the start and the end
-// of a CUDA stream capture, where allocation calls are illegal. They also
-// may not hold an ep_handle, whose workspace is an allocation. This entry
+// device memory after start-up, and plug-ins hosted by an inference runtime
+// that forbids allocations of their own. They also may not hold an
+// ep_handle, whose workspace is an allocation. This entry
 // point needs neither: the caller passes the ids, the expert outputs and the
 // result buffers, and the only scratch -- the destination-rank bit set of
 // every slot -- lives in a file-scope __device__ array of fixed size that
@@ -78,7 +77,9 @@ __global__ void noalloc_route_kernel(const __grid_constant__ NoallocRouteArgs a)
 bool is_aligned(const void *p, size_t n) { return (reinterpret_cast<uintptr_t>(p) % n) == 0; }
 
 // Device address of g_noalloc_route on the current device, looked up once
-// per device (with that device current) and cached.
+// per device (with that device current) and cached for the life of the
+// process, on the assumption that the device's primary context lives as long
+// as the process.
 ep_status route_scratch(uint64_t **out)
 {
     int dev = -1;
@@ -114,6 +115,15 @@ int sm_count_here()
 }
 
 }  // namespace
+
+cudaError_t epk::noalloc_binary_version(int *out)
+{
+    cudaFuncAttributes attr;
+    cudaError_t ce = cudaFuncGetAttributes(&attr, reinterpret_cast<const void *>(noalloc_route_kernel));
+    if (ce == cudaSuccess)
+        *out = attr.binaryVersion;
+    return ce;
+}
 
 extern "C" ep_status ep_combine_noalloc(int ep_size, int num_experts, int top_k, int hidden,
                                         int tokens_per_rank, const int32_t *num_tokens,

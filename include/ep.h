@@ -55,8 +55,10 @@
  * (state, results of the accesses that were inside) stand. Inside a stream
  * capture the wait is skipped and the record is reported by the next call
  * outside one. All calls of the library share one record per device, so
- * overlapping work on two streams may report the other's access. It is
- * for testing: slower, and synchronous.
+ * overlapping work on two streams may report the other's access; its device
+ * address is looked up once per device and kept, which assumes the primary
+ * context lives as long as the process. It is for testing: slower, and
+ * synchronous.
  */
 #ifndef EP_GB300_H
 #define EP_GB300_H
@@ -273,15 +275,23 @@ uint64_t ep_rank_mask(const int *ranks, int n);
 /* Message of the calling thread's last failed call ("" if none). */
 const char *ep_last_error(void);
 
+/* The architecture of the device code the CUDA runtime loaded for this
+ * library on the current device: *version = major*10 + minor of the binary
+ * (103 for the sm_103a build), as cudaFuncGetAttributes reports it for every
+ * kernel of the library. EP_ERR_CUDA when the kernels cannot be loaded on
+ * the current device (e.g. no sm_103 GPU), EP_ERR_UNSUPPORTED when two
+ * kernels report different versions. Runs no kernel. (Not on the pages: a
+ * build check.) */
+ep_status ep_binary_version(int *version);
+
 /* Largest ep_size * tokens_per_rank that ep_combine_noalloc accepts. */
 #define EP_NOALLOC_MAX_SLOTS 65536
 
 /* Combine for callers that cannot allocate device memory. The pages have no
  * counterpart: it exists for code that may not call cudaMalloc or any
- * allocator where it combines (inside an arena that owns all device memory,
- * a plug-in of a runtime that forbids its own allocations, or between the
- * start and end of a stream capture) and that holds no ep_handle, whose
- * workspace is an allocation.
+ * allocator where it combines (code inside an arena that owns all device
+ * memory after start-up, or a plug-in of a runtime that forbids allocations
+ * of its own) and that holds no ep_handle, whose workspace is an allocation.
  *
  * It computes what ep_combine computes, from the same ids instead of a
  * pending dispatch: output[s][t] = bf16( sum over the active ranks d that own
@@ -303,8 +313,10 @@ const char *ep_last_error(void);
  * array: calls whose GPU work overlaps (e.g. on two streams) race.
  * The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call
- * before any stream capture. It calls no allocator: no cudaMalloc, no
- * cudaFree, no allocating library routine. */
+ * before any stream capture. The address is kept for the rest of the
+ * process: this assumes the device's primary context lives as long as the
+ * process (after a cudaDeviceReset the kept address is stale). It calls no
+ * allocator: no cudaMalloc, no cudaFree, no allocating library routine. */
 ep_status ep_combine_noalloc(int ep_size, int num_experts, int top_k, int hidden,
                              int tokens_per_rank, const int32_t *num_tokens,
                              const int32_t *const *topk_ids, uint64_t active_rank_mask,

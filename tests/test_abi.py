@@ -27,11 +27,23 @@ def test_header_and_exports_agree():
         assert hasattr(L, name), name
 
 
-def test_library_is_built_for_sm103a():
+def test_library_is_the_in_tree_build():
     path = _lib.load()._name
     assert os.path.basename(path) == os.path.basename(_lib.lib_path())
     assert os.path.basename(path) in ("libep_gb300.so", "libep_gb300_checked.so")
     assert os.path.dirname(path).endswith(os.path.join("combine_topk_ids_dest_gb300", "_build"))
+
+
+@pytest.mark.gpu
+def test_loaded_kernels_are_sm103a_code(cuda_device):
+    """The runtime's own report (cudaFuncGetAttributes.binaryVersion) for every
+    kernel of the loaded library: code built for sm_103."""
+    import torch
+    torch.cuda.set_device(cuda_device)
+    v = ctypes.c_int(0)
+    L = _lib.load()
+    assert L.ep_binary_version(ctypes.byref(v)) == ep.EP_OK, L.ep_last_error()
+    assert v.value == 103
 
 
 def _size(*args):

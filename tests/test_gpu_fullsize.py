@@ -1,42 +1,23 @@
 """GPU parity at the workloads' full sizes, through the same EpComm/C-ABI
-launch path the bench times.
+launch path the bench times: every token is compared with the oracle.
 
-- The whole receive id plane of every rank is compared with the oracle's
-  (cheap at any size).
-- A sample of source tokens (every rank represented, first and last slots
-  included) is rebuilt as a small problem for the oracle; its receive rows and
-  combine outputs must equal the GPU's rows for the same tokens bit for bit.
-- Property at any size: a token's output is exactly the ordered fp32 sum of
-  the stand-in expert rows of the ranks the oracle routes it to.
+- The whole receive id plane of every rank is compared with the oracle's.
+- Every token of every source rank is then compared bit for bit: its
+  routed hidden, scale and weight rows in each rank it reaches, and its
+  combine output. The oracle works through the tokens in chunks (tokens
+  [t0, t0+Tm) of every rank as a problem of its own, see ep_chunked.py) on a
+  pool of host processes; the chunks together cover the whole workload.
 """
 import numpy as np
 import pytest
 import torch
 
+import ep_chunked
 import oracle
 import workloads
-from ep_testutil import EO_SEED, INV, fill_expert_outputs, out_bits, raw_bytes, to_dev
+from ep_testutil import fill_expert_outputs, out_bits, raw_bytes, to_dev
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
-
-SAMPLE = 256
-
-
-def _sample_slots(inp, rng):
-    ep = inp.wl.ep_size
-    picks = {s: set() for s in range(ep)}
-    live = [(s, t) for s in range(ep) for t in (0, inp.num_tokens[s] - 1) if inp.num_tokens[s] > 0]
-    for s, t in live:
-        picks[s].add(t)
-    total = inp.total_tokens
-    for _ in range(min(SAMPLE, total)):
-        g = int(rng.integers(0, total))
-        for s in range(ep):  # global token index -> (s, t)
-            if g < inp.num_tokens[s]:
-                picks[s].add(g)
-                break
-            g -= inp.num_tokens[s]
-    return {s: sorted(v) for s, v in picks.items()}
 
 
 # Combines whose output reaches 192 MiB take the library's 32-byte-access path;
@@ -56,15 +37,23 @@ LARGE["region_over_4gib"] = workloads.EpWorkload(
     runtime_max=None, counts=("fixed", 0, 0, 0, 16400), combine_dtype="fp32", seed=33)
 
 
-@pytest.mark.parametrize("name", ["mixtral_decode", "dsv3_decode", "dsv3_prefill", "qwen3_mask",
+@pytest.fixture(scope="module")
+def oracle_pool():
+    ex = ep_chunked.pool()
+    try:
+        yield ex
+    finally:
+        ex.shutdown(wait=True, cancel_futures=True)
+
+
+@pytest.mark.parametrize("name", ["tiny", "mixtral_decode", "dsv3_decode", "dsv3_prefill", "qwen3_mask",
                                   "large_bf16", "large_fp16", "large_fp32", "region_over_4gib"])
-def test_full_size_sampled(cuda_device, name):
+def test_full_size_every_token(cuda_device, oracle_pool, name):
     from combine_topk_ids_dest_gb300 import EpComm
     wl = workloads.WORKLOADS[name] if name in workloads.WORKLOADS else LARGE[name]
     inp = workloads.make_inputs(wl)
     ep, E, K, H = wl.ep_size, wl.num_experts, wl.top_k, wl.hidden
-    dtype = wl.torch_dtype
-    comm = EpComm(ep, E, K, H, wl.capacity, dtype=dtype, enable_rank_mask=wl.enable_rank_mask,
+    comm = EpComm(ep, E, K, H, wl.capacity, dtype=wl.torch_dtype, enable_rank_mask=wl.enable_rank_mask,
                   device=cuda_device, combine_dtype=wl.combine_torch_dtype)
     try:
         mask = inp.active_rank_mask if wl.enable_rank_mask else None
@@ -81,61 +70,30 @@ def test_full_size_sampled(cuda_device, name):
         want_ids = oracle.dispatch(ep, E, K, T, inp.num_tokens, inp.hidden, inp.topk_ids,
                                    mask_enabled=wl.enable_rank_mask,
                                    active_rank_mask=inp.active_rank_mask, payload=False).recv_ids
+        ids_host = [res.topk_ids[d].cpu().numpy() for d in range(ep)]
         for d in range(ep):
-            np.testing.assert_array_equal(res.topk_ids[d].cpu().numpy(), want_ids[d],
-                                          err_msg=f"id plane of rank {d}")
+            np.testing.assert_array_equal(ids_host[d], want_ids[d], err_msg=f"id plane of rank {d}")
+        del want_ids
 
-        # 2. sampled tokens as a small oracle problem
-        picks = _sample_slots(inp, np.random.default_rng(5))
-        Tm = max(1, max(len(v) for v in picks.values()))
-        def sub(lst, s):  # rows of the sampled tokens (fp8 rows indexed as raw bytes)
-            if lst is None:
-                return None
-            x = lst[s].view(torch.uint8) if lst[s].dtype == torch.float8_e4m3fn else lst[s]
-            return x[torch.tensor(picks[s], dtype=torch.long)]
-        m_hidden = [sub(inp.hidden, s) for s in range(ep)]
-        m_ids = [sub(inp.topk_ids, s) for s in range(ep)]
-        m_w = None if inp.topk_weights is None else [sub(inp.topk_weights, s) for s in range(ep)]
-        m_sc = None if inp.scale is None else [sub(inp.scale, s) for s in range(ep)]
-        m_counts = [len(picks[s]) for s in range(ep)]
-        # mini row s*Tm+j stands for full row s*T+picks[s][j]
-        full_rows = np.zeros(ep * Tm, np.int64)
-        for s in range(ep):
-            for j, t in enumerate(picks[s]):
-                full_rows[s * Tm + j] = s * T + t
-        disp = oracle.dispatch(ep, E, K, Tm, m_counts, m_hidden, m_ids, scale=m_sc, topk_weights=m_w,
-                               mask_enabled=wl.enable_rank_mask, active_rank_mask=inp.active_rank_mask,
-                               row_bytes=H * wl.elem_bytes, scale_cols=wl.scale_cols)
-        rows_t = torch.from_numpy(full_rows)
-        eo = [out_bits(workloads.expert_output_rows(EO_SEED, d, rows_t, H, dtype=wl.combine_dtype))
-              for d in range(ep)]
-        mout = oracle.combine_typed(ep, E, K, H, Tm, m_counts, m_ids, eo, wl.combine_dtype,
-                                    mask_enabled=wl.enable_rank_mask,
-                              active_rank_mask=inp.active_rank_mask)
+        # 2. every token, chunk by chunk, on the oracle pool
+        g = ep_chunked.Geometry(ep=ep, E=E, K=K, H=H, T=T, row_bytes=H * wl.elem_bytes,
+                                scale_cols=wl.scale_cols, combine_dtype=wl.combine_dtype,
+                                mask_enabled=wl.enable_rank_mask, active_rank_mask=inp.active_rank_mask)
+        Tm = ep_chunked.chunk_tokens(g)
+        n_chunks = len(ep_chunked.chunk_starts(inp.num_tokens, Tm))
+        bufs = {"hidden": res.hidden_states, "scale": res.hidden_states_scale, "weights": res.topk_weights}
 
-        live = np.array([j < m_counts[s] for s in range(ep) for j in range(Tm)])
-        idx = torch.from_numpy(full_rows[live]).to(cuda_device)
-        for d in range(ep):
-            want = disp.recv_ids[d][live]
-            np.testing.assert_array_equal(res.topk_ids[d].index_select(0, idx).cpu().numpy(), want)
-            valid = (want != INV).any(axis=1)
-            got_h = raw_bytes(res.hidden_states[d].index_select(0, idx).cpu())
-            np.testing.assert_array_equal(got_h[valid], disp.recv_hidden[d][live][valid])
-            if m_sc is not None:
-                got = res.hidden_states_scale[d].index_select(0, idx).cpu().numpy()
-                np.testing.assert_array_equal(got[valid].view(np.uint32),
-                                              disp.recv_scale[d][live][valid].view(np.uint32))
-            if m_w is not None:
-                got = res.topk_weights[d].index_select(0, idx).cpu().numpy()
-                np.testing.assert_array_equal(got[valid].view(np.uint32),
-                                              disp.recv_weights[d][live][valid].view(np.uint32))
-        for s in range(ep):
-            if not picks[s]:
-                continue
-            ts = torch.tensor(picks[s], dtype=torch.long, device=cuda_device)
-            got = out_bits(out[s].index_select(0, ts).cpu())
-            if got.dtype == np.uint32:
-                mout[s] = mout[s].view(np.uint32)
-            np.testing.assert_array_equal(got, mout[s], err_msg=f"combine output of rank {s}")
+        def rows_of(kind, d, rows):
+            x = bufs[kind][d].index_select(0, torch.from_numpy(rows).to(cuda_device)).cpu()
+            return raw_bytes(x) if kind == "hidden" else x.numpy()
+
+        def out_of(s, t0, m):
+            return out_bits(out[s][t0:t0 + m].cpu())
+
+        jobs = ep_chunked.make_jobs(g, inp, ids_host, Tm, rows_of, out_of, res.hidden_states_scale is not None,
+                                    res.topk_weights is not None)
+        checked = ep_chunked.run_jobs(oracle_pool, jobs, in_flight=2 * oracle_pool._max_workers)
+        assert checked == n_chunks
+        assert n_chunks * Tm >= max(inp.num_tokens)  # the chunks reach every rank's last token
     finally:
         comm.destroy()
