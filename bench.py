@@ -512,7 +512,7 @@ def run_ours(args, rank, world):
     b = round_bytes(inp)
     dtype = wl.torch_dtype
     comm = EpComm(wl.ep_size, wl.num_experts, wl.top_k, wl.hidden, wl.capacity, dtype=dtype,
-                  enable_rank_mask=wl.enable_rank_mask, device=dev)
+                  enable_rank_mask=wl.enable_rank_mask, device=dev, pdl=args.pdl)
     mask = inp.active_rank_mask if wl.enable_rank_mask else None
     hid = [x.to(dev) for x in inp.hidden]
     ids = [x.to(dev) for x in inp.topk_ids]
@@ -642,6 +642,7 @@ def run_ours(args, rank, world):
                   "separate graphs in a second pass, events around each",
         "us_per_round_two_graphs": 1e3 * statistics.mean(t_split),
         "gpu_launches": launches_per_round * args.steps,
+        "launch": "programmatic dependent launch (EP_LAUNCH_PDL)" if args.pdl else "stream order",
         "clocks": clocks.summary(),
     }
     if world == 1 and not args.no_cpu_baseline:
@@ -777,6 +778,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--l2-flush", default="write+read", choices=["write", "write+read"],
                     help="how L2 is evicted between timed steps")
+    ap.add_argument("--pdl", action=argparse.BooleanOptionalAction, default=False,
+                    help="launch the kernels with programmatic dependent launch")
     ap.add_argument("--tokens-per-rank", type=int, default=None,
                     help="shrink the workload to this many tokens per rank (profiling runs only)")
     args = ap.parse_args()

@@ -32,6 +32,7 @@ EP_DTYPE_FP8_E4M3 = 1
 EP_DTYPE_FP16 = 2
 EP_DTYPE_FP32 = 3
 EP_SCALE_COLS_DEFAULT = -1
+EP_LAUNCH_PDL = 1
 EP_INVALID_EXPERT_ID = -1
 EP_MAX_EP_SIZE = 64
 EP_MAX_TOP_K = 32
@@ -61,7 +62,8 @@ class EpConfigC(ctypes.Structure):
     _fields_ = [("ep_size", ctypes.c_int), ("num_experts", ctypes.c_int), ("top_k", ctypes.c_int),
                 ("hidden", ctypes.c_int), ("max_tokens_per_rank", ctypes.c_int), ("dtype", ctypes.c_int),
                 ("enable_rank_mask", ctypes.c_int), ("scale_cols", ctypes.c_int),
-                ("eplb_stats_max_bytes", ctypes.c_int), ("combine_dtype", ctypes.c_int)]
+                ("eplb_stats_max_bytes", ctypes.c_int), ("combine_dtype", ctypes.c_int),
+                ("launch_flags", ctypes.c_int)]
 
 
 class EpDispatchArgsC(ctypes.Structure):

@@ -44,6 +44,7 @@ struct ep_handle {
     ep_dtype combine_dtype;
     int mask_enabled;
     int eplb_max_bytes;
+    bool pdl;  // EP_LAUNCH_PDL
     int device;
 
     uint8_t *ws;
@@ -123,6 +124,7 @@ ep_config default_config(int ep, int E, int K, int H, int C, ep_dtype dtype, int
     c.scale_cols = EP_SCALE_COLS_DEFAULT;
     c.eplb_stats_max_bytes = 0;
     c.combine_dtype = EP_DTYPE_BF16;
+    c.launch_flags = 0;
     return c;
 }
 
@@ -163,6 +165,8 @@ ep_status plan(const ep_config *cfg, Layout *L)
     if (cfg->eplb_stats_max_bytes < 0 || cfg->eplb_stats_max_bytes % 4 != 0)
         return fail(EP_ERR_INVALID_ARG, "eplb_stats_max_bytes=%d must be a non-negative multiple of 4",
                     cfg->eplb_stats_max_bytes);
+    if (cfg->launch_flags & ~EP_LAUNCH_PDL)
+        return fail(EP_ERR_INVALID_ARG, "launch_flags=0x%x has unknown bits", (unsigned)cfg->launch_flags);
     L->elem_bytes = elem;
     L->row_bytes = H * elem;
     if (cfg->scale_cols == EP_SCALE_COLS_DEFAULT)
@@ -253,6 +257,7 @@ ep_status make_handle(const ep_config *cfg, void *ws, size_t ws_bytes, bool own,
     h->scale_cols = L.scale_cols;
     h->mask_enabled = cfg->enable_rank_mask ? 1 : 0;
     h->eplb_max_bytes = cfg->eplb_stats_max_bytes;
+    h->pdl = (cfg->launch_flags & EP_LAUNCH_PDL) != 0;
     h->combine_dtype = cfg->combine_dtype;
     h->device = dev;
     h->ws = static_cast<uint8_t *>(ws);
@@ -612,7 +617,7 @@ ep_status ep_dispatch_ex(ep_handle *h, const ep_dispatch_args *args, void *strea
     a.chk = epk::check_ctx(rec);
 
     nvtxRangePushA("ep_dispatch");  // host-side range around the launch, for profilers
-    cudaError_t ce = epk::launch_dispatch(a, static_cast<cudaStream_t>(stream));
+    cudaError_t ce = epk::launch_dispatch(a, static_cast<cudaStream_t>(stream), h->pdl);
     nvtxRangePop();
     if (ce != cudaSuccess)
         return fail(EP_ERR_CUDA, "dispatch launch: %s", cudaGetErrorString(ce));
@@ -705,7 +710,7 @@ ep_status ep_combine(ep_handle *h, const void *const *expert_output, void *const
     a.chk = epk::check_ctx(rec);
 
     nvtxRangePushA("ep_combine");
-    cudaError_t ce = epk::launch_combine(a, static_cast<cudaStream_t>(stream));
+    cudaError_t ce = epk::launch_combine(a, static_cast<cudaStream_t>(stream), h->pdl);
     nvtxRangePop();
     if (ce != cudaSuccess)
         return fail(EP_ERR_CUDA, "combine launch: %s", cudaGetErrorString(ce));

@@ -141,9 +141,12 @@ ep_status set_error(ep_status st, const char *fmt, ...);
 cudaError_t kernel_binary_versions(int *out, int max, int *n);
 cudaError_t noalloc_binary_version(int *out);
 
-// Queue one launch on `stream`; returns the launch's cudaError_t.
-cudaError_t launch_dispatch(const DispatchArgs &a, cudaStream_t stream);
-cudaError_t launch_combine(const CombineArgs &a, cudaStream_t stream);
+// Queue one launch on `stream`; returns the launch's cudaError_t. `pdl`:
+// launch with programmatic dependent launch (EP_LAUNCH_PDL); the kernels
+// wait for their predecessor with griddepcontrol.wait before touching global
+// memory either way (a no-op without the launch attribute).
+cudaError_t launch_dispatch(const DispatchArgs &a, cudaStream_t stream, bool pdl);
+cudaError_t launch_combine(const CombineArgs &a, cudaStream_t stream, bool pdl);
 
 // Checked build: the CheckCtx for a launch recording into `rec`, with the
 // test hook's trim applied; and, after the launch, EP_OK or

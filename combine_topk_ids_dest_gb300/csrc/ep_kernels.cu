@@ -78,6 +78,14 @@ constexpr int kCombineMaxThreads = EP_COMBINE_MAX_THREADS;
 constexpr int kCombineVpt = EP_COMBINE_VPT;      // 16-byte column vectors per combine thread
 constexpr int kCombineBatch = EP_COMBINE_BATCH;  // ranks whose rows are loaded before their adds
 
+// Programmatic dependent launch (sm_90+). launch_dependents: the next kernel
+// of the stream may be scheduled once every block of this grid has issued it
+// (or exited). wait: block until the previous kernel of the stream has
+// completed and its memory operations are visible. Both are no-ops when the
+// grid was launched without the programmatic-serialization attribute.
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ uint4 ld_stream(const void *p)
 {
     uint4 v;
@@ -223,6 +231,10 @@ __global__ void __launch_bounds__(kDispatchThreads)
     const long long n_slots = (long long)a.ep * a.T;
     const long long warp_stride = (long long)gridDim.x * wpb;
     const int K = a.top_k;
+    // Nothing below may touch global memory before the previous kernel is done:
+    // it may have produced the inputs, or still read the buffers written here.
+    pdl_launch_dependents();
+    pdl_wait();
 
     // ---- eplb_local_stats all-gather: warp r copies rank r's statistics
     // into row r of the gathered buffer (a few hundred bytes per rank).
@@ -429,6 +441,9 @@ __global__ void __launch_bounds__(kCombineMaxThreads)
     const long long row_bytes = (long long)a.H * (16 / kEpv);
     const int nvec = (int)(row_bytes / VB);
     const int nthr = blockDim.x;
+    // the routing state and the expert outputs come from the kernels before this one
+    pdl_launch_dependents();
+    pdl_wait();
     for (long long b = blockIdx.x; b < n_blocks; b += gridDim.x) {
         // block -> (live token g, column chunk); g -> source rank s by binary
         // search of the token offsets, so no block is spent on padding slots
@@ -533,6 +548,24 @@ __global__ void __launch_bounds__(kCombineMaxThreads)
 // threads*VPT; a width whose chunks tile the row exactly leaves no idle
 // threads (64 for 4096-wide rows, 32 for 7168-wide rows). Preference order
 // from measurements on GB300.
+// One launch of `kernel` on `stream`, with programmatic dependent launch
+// when `pdl` is set.
+template <typename Kernel, typename... Args>
+cudaError_t launch(Kernel kernel, long long grid, int threads, cudaStream_t stream, bool pdl, Args... args)
+{
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3((unsigned)threads, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 int combine_threads(int nvec)
 {
     const int per_thread = kCombineVpt;
@@ -587,7 +620,7 @@ cudaError_t kernel_binary_versions(int *out, int max, int *n)
     return cudaSuccess;
 }
 
-cudaError_t launch_dispatch(const DispatchArgs &a, cudaStream_t stream)
+cudaError_t launch_dispatch(const DispatchArgs &a, cudaStream_t stream, bool pdl)
 {
     const long long n_slots = (long long)a.ep * a.T;
     if (n_slots == 0 && a.eplb_bytes == 0)
@@ -609,14 +642,12 @@ cudaError_t launch_dispatch(const DispatchArgs &a, cudaStream_t stream)
     const long long eplb_blocks = a.eplb_bytes > 0 ? (a.ep + wpb - 1) / wpb : 0;  // one warp per rank
     if (blocks < eplb_blocks)
         blocks = eplb_blocks;
-    if (wide)
-        dispatch_kernel<32><<<(unsigned)blocks, kDispatchThreads, 0, stream>>>(a);
-    else
-        dispatch_kernel<16><<<(unsigned)blocks, kDispatchThreads, 0, stream>>>(a);
-    return cudaGetLastError();
+    cudaError_t ce = wide ? launch(dispatch_kernel<32>, blocks, kDispatchThreads, stream, pdl, a)
+                          : launch(dispatch_kernel<16>, blocks, kDispatchThreads, stream, pdl, a);
+    return ce != cudaSuccess ? ce : cudaGetLastError();
 }
 
-cudaError_t launch_combine(const CombineArgs &a, cudaStream_t stream)
+cudaError_t launch_combine(const CombineArgs &a, cudaStream_t stream, bool pdl)
 {
     const int elem = a.ctype == EP_DTYPE_FP32 ? 4 : 2;
     const int nvec = (int)(((long long)a.H * elem) >> 4);
@@ -642,24 +673,25 @@ cudaError_t launch_combine(const CombineArgs &a, cudaStream_t stream)
     for (int s = 0; wide && s < a.ep; ++s)
         if (a.num_tokens[s] > 0 && (reinterpret_cast<uintptr_t>(a.out[s]) % 32) != 0)
             wide = false;
-#define EP_LAUNCH_COMBINE(CT)                                                                   \
-    (wide ? (combine_kernel<CT, 32><<<(unsigned)grid, threads, 0, stream>>>(a, bpr, n_blocks), 0) \
-          : (combine_kernel<CT, 16><<<(unsigned)grid, threads, 0, stream>>>(a, bpr, n_blocks), 0))
+#define EP_LAUNCH_COMBINE(CT)                                                          \
+    (wide ? launch(combine_kernel<CT, 32>, grid, threads, stream, pdl, a, bpr, n_blocks) \
+          : launch(combine_kernel<CT, 16>, grid, threads, stream, pdl, a, bpr, n_blocks))
+    cudaError_t ce;
     switch (a.ctype) {
     case EP_DTYPE_BF16:
-        EP_LAUNCH_COMBINE(EP_DTYPE_BF16);
+        ce = EP_LAUNCH_COMBINE(EP_DTYPE_BF16);
         break;
     case EP_DTYPE_FP16:
-        EP_LAUNCH_COMBINE(EP_DTYPE_FP16);
+        ce = EP_LAUNCH_COMBINE(EP_DTYPE_FP16);
         break;
     case EP_DTYPE_FP32:
-        EP_LAUNCH_COMBINE(EP_DTYPE_FP32);
+        ce = EP_LAUNCH_COMBINE(EP_DTYPE_FP32);
         break;
     default:
         return cudaErrorInvalidValue;
     }
 #undef EP_LAUNCH_COMBINE
-    return cudaGetLastError();
+    return ce != cudaSuccess ? ce : cudaGetLastError();
 }
 
 }  // namespace epk

@@ -218,7 +218,7 @@ extern "C" ep_status ep_combine_noalloc(int ep_size, int num_experts, int top_k,
     cudaError_t ce = cudaGetLastError();
     if (ce != cudaSuccess)
         return epk::set_error(EP_ERR_CUDA, "ep_combine_noalloc routing launch: %s", cudaGetErrorString(ce));
-    ce = epk::launch_combine(c, s);  // the library's combine, reading the static routing array
+    ce = epk::launch_combine(c, s, false);  // the library's combine, reading the static routing array
     if (ce != cudaSuccess)
         return epk::set_error(EP_ERR_CUDA, "ep_combine_noalloc combine launch: %s", cudaGetErrorString(ce));
     st = epk::check_after(rec, s, "ep_combine_noalloc");

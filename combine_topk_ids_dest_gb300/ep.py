@@ -84,7 +84,10 @@ class EpComm:
     fp32 scales per row (default hidden/128 when that divides, else none).
     ``eplb_stats_max_bytes`` reserves room to all-gather that many bytes of
     ``eplb_local_stats`` per rank. ``combine_dtype`` (bf16, fp16 or fp32)
-    is the type of the expert outputs combine sums and of its results. The
+    is the type of the expert outputs combine sums and of its results.
+    ``pdl`` launches the kernels with programmatic dependent launch
+    (``EP_LAUNCH_PDL``): a combine queued right after its dispatch is
+    scheduled while the dispatch drains; results are unchanged. The
     workspace is allocated here with torch, at capacity
     ``max_tokens_per_rank``.
 
@@ -95,7 +98,8 @@ class EpComm:
     def __init__(self, ep_size: int, num_experts: int, top_k: int, hidden: int,
                  max_tokens_per_rank: int, dtype: torch.dtype = torch.bfloat16,
                  enable_rank_mask: bool = False, device=None, scale_cols: Optional[int] = None,
-                 eplb_stats_max_bytes: int = 0, combine_dtype: torch.dtype = torch.bfloat16):
+                 eplb_stats_max_bytes: int = 0, combine_dtype: torch.dtype = torch.bfloat16,
+                 pdl: bool = False):
         self._L = _lib.load()
         if dtype not in _DTYPES:
             raise ValueError(f"dtype {dtype} not supported (bfloat16, float8_e4m3fn, float16, float32)")
@@ -112,9 +116,11 @@ class EpComm:
         if combine_dtype not in _COMBINE_DTYPES:
             raise ValueError(f"combine_dtype {combine_dtype} not supported (bfloat16, float16, float32)")
         self.combine_dtype = combine_dtype
+        self.pdl = bool(pdl)
         cfg = _lib.EpConfigC(self.ep_size, self.num_experts, self.top_k, self.hidden,
                              self.max_tokens_per_rank, _DTYPES[dtype], int(self.enable_rank_mask),
-                             self.scale_cols, self.eplb_stats_max_bytes, _DTYPES[combine_dtype])
+                             self.scale_cols, self.eplb_stats_max_bytes, _DTYPES[combine_dtype],
+                             _lib.EP_LAUNCH_PDL if self.pdl else 0)
         nbytes = ctypes.c_size_t(0)
         check(self._L.ep_workspace_size_ex(ctypes.byref(cfg), ctypes.byref(nbytes)))
         with torch.cuda.device(self.device):

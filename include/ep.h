@@ -131,7 +131,23 @@ typedef struct {
     ep_dtype combine_dtype;    /* type of the expert outputs combine sums and of its results:
                                   EP_DTYPE_BF16 (0, the default), EP_DTYPE_FP16 or EP_DTYPE_FP32;
                                   hidden*elem_bytes of it must be a multiple of 16 */
+    int launch_flags;          /* 0 or EP_LAUNCH_PDL (below) */
 } ep_config;
+
+/* ep_config.launch_flags bit: launch the dispatch and combine kernels with
+ * programmatic dependent launch (cudaLaunchAttributeProgrammaticStream-
+ * Serialization). Each kernel lets the next kernel of its stream be launched
+ * as soon as all of its own blocks are running, and itself waits
+ * (griddepcontrol.wait) for the kernel before it to complete and its memory
+ * to be visible before touching global memory. So a combine queued right
+ * after its dispatch is launched and scheduled while the dispatch drains,
+ * and results are the same as with ordinary stream order. A kernel before
+ * it that does not let dependents launch early (any ordinary kernel) is
+ * simply waited for, so the flag is safe with any producer on the stream.
+ * Also honoured inside stream capture (the graph keeps the programmatic
+ * edge). Not on the pages: a launch-latency option for small (decode-size)
+ * rounds. */
+#define EP_LAUNCH_PDL 1
 
 /* Everything one dispatch takes (ep_dispatch_ex); see ep_dispatch for the
  * first seven fields. eplb_local_stats: NULL, or eplb_local_stats[r] =
@@ -199,8 +215,8 @@ ep_status ep_create_with_workspace(int ep_size, int num_experts, int top_k, int 
 /* Creates a handle from a full configuration. workspace == NULL: allocate
  * with cudaMalloc (freed by ep_destroy); else caller-owned device memory of
  * `bytes` >= ep_workspace_size_ex, 256-byte aligned. ep_create(...) equals
- * ep_create_ex with scale_cols = EP_SCALE_COLS_DEFAULT and
- * eplb_stats_max_bytes = 0. */
+ * ep_create_ex with scale_cols = EP_SCALE_COLS_DEFAULT,
+ * eplb_stats_max_bytes = 0 and launch_flags = 0. */
 ep_status ep_create_ex(const ep_config *cfg, void *workspace, size_t bytes, ep_handle **out);
 
 /* Dispatch of all ep_size source ranks (MoEEpCommunication.dispatch;

@@ -81,11 +81,12 @@ def fill_expert_outputs(comm, T, device, seed=EO_SEED, special=False, caller=Fal
     return outs if caller else None
 
 
-def gpu_round(inp, device, special=False, caller_eo=False, comm=None, keep=False, dev_counts=None):
+def gpu_round(inp, device, special=False, caller_eo=False, comm=None, keep=False, dev_counts=None, pdl=False):
     """dispatch + (stand-in expert) + combine of ``inp`` through EpComm.
     Returns host copies of the receive buffers and outputs. ``dev_counts``
     (a list of ints) is passed as device-side token counts; the outputs are
-    then cut to the counts clamped to [0, the rank's rows]."""
+    then cut to the counts clamped to [0, the rank's rows]. ``pdl``: a
+    communicator created here launches with programmatic dependent launch."""
     from combine_topk_ids_dest_gb300 import EpComm
     wl = inp.wl
     own = comm is None
@@ -93,7 +94,7 @@ def gpu_round(inp, device, special=False, caller_eo=False, comm=None, keep=False
         comm = EpComm(wl.ep_size, wl.num_experts, wl.top_k, wl.hidden, wl.capacity, dtype=wl.torch_dtype,
                       enable_rank_mask=wl.enable_rank_mask, device=device,
                       scale_cols=wl.scale_cols if wl.scales else None,
-                      combine_dtype=wl.combine_torch_dtype)
+                      combine_dtype=wl.combine_torch_dtype, pdl=pdl)
     mask = inp.active_rank_mask if wl.enable_rank_mask else None
     res = comm.dispatch(to_dev(inp.hidden, device), to_dev(inp.topk_ids, device),
                         to_dev(inp.topk_weights, device),

@@ -129,7 +129,7 @@ def test_create_without_gpu_reports_error():
 
 def _size_ex(**kw):
     base = dict(ep_size=4, num_experts=8, top_k=2, hidden=256, max_tokens_per_rank=16, dtype=0,
-                enable_rank_mask=0, scale_cols=-1, eplb_stats_max_bytes=0, combine_dtype=0)
+                enable_rank_mask=0, scale_cols=-1, eplb_stats_max_bytes=0, combine_dtype=0, launch_flags=0)
     base.update(kw)
     cfg = _lib.EpConfigC(*[base[f] for f, _ in _lib.EpConfigC._fields_])
     n = ctypes.c_size_t(0)
@@ -172,6 +172,12 @@ def test_combine_dtype_rules():
 
 def test_default_config_matches_plain_workspace_size():
     assert _size_ex() == _size(4, 8, 2, 256, 16, 0)
+
+
+def test_launch_flags():
+    assert _size_ex(launch_flags=_lib.EP_LAUNCH_PDL) == _size_ex()  # no workspace of its own
+    st, _ = _size_ex(launch_flags=2)
+    assert st == ep.EP_ERR_INVALID_ARG and b"launch_flags" in _lib.load().ep_last_error()
 
 
 @pytest.mark.parametrize("kw,frag", [

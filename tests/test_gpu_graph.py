@@ -20,10 +20,11 @@ from ep_testutil import EO_SEED, INV, bf16_bits, raw_bytes
 pytestmark = pytest.mark.gpu
 
 
-def test_captured_round_replays_with_new_inputs(cuda_device):
+@pytest.mark.parametrize("pdl", [False, True], ids=["stream_order", "pdl"])
+def test_captured_round_replays_with_new_inputs(cuda_device, pdl):
     ep, E, K, H, C = 8, 64, 6, 512, 24
     dev = cuda_device
-    comm = EpComm(ep, E, K, H, C, dtype=torch.float8_e4m3fn, enable_rank_mask=True, device=dev)
+    comm = EpComm(ep, E, K, H, C, dtype=torch.float8_e4m3fn, enable_rank_mask=True, device=dev, pdl=pdl)
     try:
         hid = [torch.zeros(C, H, dtype=torch.float8_e4m3fn, device=dev) for _ in range(ep)]
         scl = [torch.ones(C, H // 128, device=dev) for _ in range(ep)]
