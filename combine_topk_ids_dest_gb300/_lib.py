@@ -43,13 +43,16 @@ ALL_RANKS = (1 << 64) - 1  # "no mask": every rank active
 EXPORTS = ("ep_is_supported", "ep_workspace_size", "ep_create", "ep_create_with_workspace",
            "ep_dispatch", "ep_get_combine_input_buffer", "ep_combine", "ep_destroy",
            "ep_rank_mask", "ep_last_error", "ep_combine_noalloc", "ep_workspace_size_ex",
-           "ep_create_ex", "ep_dispatch_ex", "ep_binary_version")
+           "ep_create_ex", "ep_dispatch_ex", "ep_binary_version", "ep_partition_describe",
+           "ep_partition_check", "ep_partition_connect")
 EP_NOALLOC_MAX_SLOTS = 65536
 
 
 class EpDispatchResultC(ctypes.Structure):
     _fields_ = [("tokens_per_rank", ctypes.c_int),
                 ("ep_size", ctypes.c_int),
+                ("first_rank", ctypes.c_int),
+                ("num_ranks", ctypes.c_int),
                 ("recv_hidden", ctypes.POINTER(ctypes.c_void_p)),
                 ("recv_scale", ctypes.POINTER(ctypes.c_void_p)),
                 ("recv_topk_ids", ctypes.POINTER(ctypes.c_void_p)),
@@ -63,7 +66,16 @@ class EpConfigC(ctypes.Structure):
                 ("hidden", ctypes.c_int), ("max_tokens_per_rank", ctypes.c_int), ("dtype", ctypes.c_int),
                 ("enable_rank_mask", ctypes.c_int), ("scale_cols", ctypes.c_int),
                 ("eplb_stats_max_bytes", ctypes.c_int), ("combine_dtype", ctypes.c_int),
-                ("launch_flags", ctypes.c_int)]
+                ("launch_flags", ctypes.c_int), ("num_partitions", ctypes.c_int), ("partition", ctypes.c_int)]
+
+
+class EpPartitionInfoC(ctypes.Structure):
+    """ep_partition_info: one partition of a partitioned EP group as its peers see it."""
+    _fields_ = [("config", EpConfigC), ("first_rank", ctypes.c_int), ("num_ranks", ctypes.c_int),
+                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t)] + \
+        [(f, ctypes.c_size_t) for f in ("off_recv_hidden", "off_recv_scale", "off_recv_ids", "off_recv_weights",
+                                         "off_combine_in", "off_eplb", "stride_recv_hidden", "stride_recv_scale",
+                                         "stride_recv_ids", "stride_recv_weights", "stride_combine_in")]
 
 
 class EpDispatchArgsC(ctypes.Structure):
@@ -140,6 +152,12 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         L.ep_combine_noalloc.restype = i32
         L.ep_binary_version.argtypes = [ctypes.POINTER(i32)]
         L.ep_binary_version.restype = i32
+        L.ep_partition_describe.argtypes = [ctypes.POINTER(EpConfigC), P, sz, ctypes.POINTER(EpPartitionInfoC)]
+        L.ep_partition_describe.restype = i32
+        L.ep_partition_check.argtypes = [ctypes.POINTER(EpPartitionInfoC), i32]
+        L.ep_partition_check.restype = i32
+        L.ep_partition_connect.argtypes = [P, ctypes.POINTER(EpPartitionInfoC), i32]
+        L.ep_partition_connect.restype = i32
         L.ep_last_error.argtypes = []
         L.ep_last_error.restype = ctypes.c_char_p
         if checked():

@@ -15,17 +15,20 @@
 //    rank's combine-input region seen as [ep_size * tokens_per_rank, hidden].
 //
 // Workspace (one device allocation, regions 256-byte aligned, each sized at
-// capacity C = max_tokens_per_rank):
-//   recv_hidden  [ep][ep*C][row_bytes]
-//   recv_scale   [ep][ep*C][scale_cols] fp32  (scale_cols = H/128 by default)
-//   recv_ids     [ep][ep*C][K] int32
-//   recv_weights [ep][ep*C][K] fp32
-//   combine_in   [ep][ep*C][H] bf16
-//   route_mask   [ep*C] uint64
-//   live_counts  [ep] int32  (token counts of a dispatch with device-side counts)
+// capacity C = max_tokens_per_rank), for the n ranks the handle hosts (all
+// ep of them, or one partition's ep/G):
+//   recv_hidden  [n][ep*C][row_bytes]
+//   recv_scale   [n][ep*C][scale_cols] fp32  (scale_cols = H/128 by default)
+//   recv_ids     [n][ep*C][K] int32
+//   recv_weights [n][ep*C][K] fp32
+//   combine_in   [n][ep*C][H] of the combine dtype (bf16 by default)
+//   route_mask   [n*C] uint64  (routing state of the hosted source ranks' slots)
+//   live_counts  [n] int32  (token counts of a dispatch with device-side counts)
 //   eplb_stats   [ep][eplb_stats_max_bytes]  (the gathered eplb_local_stats)
 // A step with tokens_per_rank T uses the first ep*T rows of each region, so
-// receive row s*T+t of rank d sits at region base + d*stride + (s*T+t)*row.
+// receive row s*T+t of hosted rank j sits at region base + j*stride +
+// (s*T+t)*row. The kernels reach every rank's regions, this workspace's or a
+// connected partition's, through per-rank address tables held in the handle.
 #include <cstdarg>
 #include <cstdio>
 #include <cstdlib>
@@ -46,6 +49,11 @@ struct ep_handle {
     int eplb_max_bytes;
     bool pdl;  // EP_LAUNCH_PDL
     int device;
+    ep_config cfg;  // as created
+
+    // partition: hosted ranks [first, first + nloc) of num_parts (1: all ranks)
+    int num_parts, part, first, nloc;
+    bool connected;  // destination tables complete (always, unless partitioned)
 
     uint8_t *ws;
     size_t ws_bytes;
@@ -60,10 +68,19 @@ struct ep_handle {
     uint64_t mask;
     int32_t counts[EP_MAX_EP_SIZE];
 
+    // hosted ranks' receive buffers (entry j = rank first + j), for results
     void *r_hidden[EP_MAX_EP_SIZE];
     float *r_scale[EP_MAX_EP_SIZE];
     int32_t *r_ids[EP_MAX_EP_SIZE];
     float *r_weights[EP_MAX_EP_SIZE];
+
+    // every rank's buffers by global rank, and each partition's eplb buffer
+    uint8_t *t_hidden[EP_MAX_EP_SIZE];
+    float *t_scale[EP_MAX_EP_SIZE];
+    int32_t *t_ids[EP_MAX_EP_SIZE];
+    float *t_weights[EP_MAX_EP_SIZE];
+    void *t_comb[EP_MAX_EP_SIZE];
+    uint8_t *t_eplb[EP_MAX_EP_SIZE];
 };
 
 namespace {
@@ -92,6 +109,7 @@ bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 uint64_t full_mask(int ep) { return ep >= 64 ? ~0ULL : ((1ULL << ep) - 1); }
 
 struct Layout {
+    int num_parts, part, first, nloc;  // partition and hosted ranks
     int elem_bytes, row_bytes, scale_cols, combine_elem;
     size_t off_hidden, off_scale, off_ids, off_weights, off_comb, off_mask, off_counts, off_eplb, total;
     size_t st_hidden, st_scale, st_ids, st_weights, st_comb;
@@ -125,6 +143,8 @@ ep_config default_config(int ep, int E, int K, int H, int C, ep_dtype dtype, int
     c.eplb_stats_max_bytes = 0;
     c.combine_dtype = EP_DTYPE_BF16;
     c.launch_flags = 0;
+    c.num_partitions = 0;
+    c.partition = 0;
     return c;
 }
 
@@ -167,6 +187,16 @@ ep_status plan(const ep_config *cfg, Layout *L)
                     cfg->eplb_stats_max_bytes);
     if (cfg->launch_flags & ~EP_LAUNCH_PDL)
         return fail(EP_ERR_INVALID_ARG, "launch_flags=0x%x has unknown bits", (unsigned)cfg->launch_flags);
+    const int G = cfg->num_partitions <= 1 ? 1 : cfg->num_partitions;
+    if (cfg->num_partitions < 0 || ep % G != 0)
+        return fail(EP_ERR_INVALID_ARG, "num_partitions=%d must be 0, 1 or a divisor of ep_size=%d",
+                    cfg->num_partitions, ep);
+    if (cfg->partition < 0 || cfg->partition >= G)
+        return fail(EP_ERR_INVALID_ARG, "partition=%d outside [0, %d)", cfg->partition, G);
+    L->num_parts = G;
+    L->part = cfg->partition;
+    L->nloc = ep / G;
+    L->first = cfg->partition * L->nloc;
     L->elem_bytes = elem;
     L->row_bytes = H * elem;
     if (cfg->scale_cols == EP_SCALE_COLS_DEFAULT)
@@ -180,21 +210,22 @@ ep_status plan(const ep_config *cfg, Layout *L)
     L->st_weights = align256(rows * K * sizeof(float));
     L->combine_elem = ce;
     L->st_comb = align256(rows * H * ce);
+    const size_t n = (size_t)L->nloc;
     size_t off = 0;
     L->off_hidden = off;
-    off += L->st_hidden * ep;
+    off += L->st_hidden * n;
     L->off_scale = off;
-    off += L->st_scale * ep;
+    off += L->st_scale * n;
     L->off_ids = off;
-    off += L->st_ids * ep;
+    off += L->st_ids * n;
     L->off_weights = off;
-    off += L->st_weights * ep;
+    off += L->st_weights * n;
     L->off_comb = off;
-    off += L->st_comb * ep;
+    off += L->st_comb * n;
     L->off_mask = off;
-    off += align256(rows * sizeof(uint64_t));
+    off += align256(n * (size_t)C * sizeof(uint64_t));
     L->off_counts = off;
-    off += align256((size_t)ep * sizeof(int32_t));
+    off += align256(n * sizeof(int32_t));
     L->off_eplb = off;
     off += align256((size_t)ep * (size_t)cfg->eplb_stats_max_bytes);
     L->total = off < 256 ? 256 : off;
@@ -258,6 +289,12 @@ ep_status make_handle(const ep_config *cfg, void *ws, size_t ws_bytes, bool own,
     h->mask_enabled = cfg->enable_rank_mask ? 1 : 0;
     h->eplb_max_bytes = cfg->eplb_stats_max_bytes;
     h->pdl = (cfg->launch_flags & EP_LAUNCH_PDL) != 0;
+    h->cfg = *cfg;
+    h->num_parts = L.num_parts;
+    h->part = L.part;
+    h->first = L.first;
+    h->nloc = L.nloc;
+    h->connected = L.num_parts == 1;
     h->combine_dtype = cfg->combine_dtype;
     h->device = dev;
     h->ws = static_cast<uint8_t *>(ws);
@@ -280,12 +317,19 @@ ep_status make_handle(const ep_config *cfg, void *ws, size_t ws_bytes, bool own,
     h->dev_counts = false;
     h->T = 0;
     h->mask = 0;
-    for (int d = 0; d < ep; ++d) {
-        h->r_hidden[d] = h->ws + h->off_hidden + d * h->st_hidden;
-        h->r_scale[d] = reinterpret_cast<float *>(h->ws + h->off_scale + d * h->st_scale);
-        h->r_ids[d] = reinterpret_cast<int32_t *>(h->ws + h->off_ids + d * h->st_ids);
-        h->r_weights[d] = reinterpret_cast<float *>(h->ws + h->off_weights + d * h->st_weights);
+    for (int j = 0; j < h->nloc; ++j) {
+        h->r_hidden[j] = h->ws + h->off_hidden + j * h->st_hidden;
+        h->r_scale[j] = reinterpret_cast<float *>(h->ws + h->off_scale + j * h->st_scale);
+        h->r_ids[j] = reinterpret_cast<int32_t *>(h->ws + h->off_ids + j * h->st_ids);
+        h->r_weights[j] = reinterpret_cast<float *>(h->ws + h->off_weights + j * h->st_weights);
+        const int d = h->first + j;
+        h->t_hidden[d] = static_cast<uint8_t *>(h->r_hidden[j]);
+        h->t_scale[d] = h->r_scale[j];
+        h->t_ids[d] = h->r_ids[j];
+        h->t_weights[d] = h->r_weights[j];
+        h->t_comb[d] = h->ws + h->off_comb + j * h->st_comb;
     }
+    h->t_eplb[h->part] = h->ws + h->off_eplb;
     *out = h;
     return ok();
 }
@@ -522,6 +566,9 @@ ep_status ep_dispatch_ex(ep_handle *h, const ep_dispatch_args *args, void *strea
         return fail(EP_ERR_INVALID_ARG, "args is NULL");
     if (h->pending)
         return fail(EP_ERR_STATE, "dispatch called while the previous dispatch has not been combined");
+    if (!h->connected)
+        return fail(EP_ERR_STATE, "partition %d of %d is not connected with its group (ep_partition_connect)",
+                    h->part, h->num_parts);
     const void *const *hidden = args->hidden;
     const float *const *hidden_scale = args->hidden_scale;
     const int32_t *const *topk_ids = args->topk_ids;
@@ -558,7 +605,7 @@ ep_status ep_dispatch_ex(ep_handle *h, const ep_dispatch_args *args, void *strea
 
     epk::DispatchArgs a;
     std::memset(&a, 0, sizeof a);
-    for (int s = 0; s < h->ep; ++s) {
+    for (int s = 0; s < h->nloc; ++s) {  // hosted source ranks; rank h->first + s
         if (eplb_bytes) {
             if (!args->eplb_local_stats[s] || !aligned(args->eplb_local_stats[s], 4))
                 return fail(EP_ERR_INVALID_ARG, "eplb_local_stats[%d] is NULL or not 4-byte aligned "
@@ -586,17 +633,19 @@ ep_status ep_dispatch_ex(ep_handle *h, const ep_dispatch_args *args, void *strea
         a.scale[s] = hidden_scale ? hidden_scale[s] : nullptr;
         a.weights[s] = topk_weights ? topk_weights[s] : nullptr;
     }
-    a.recv_hidden = h->ws + h->off_hidden;
-    a.hidden_stride = (long long)h->st_hidden;
-    a.recv_scale = reinterpret_cast<float *>(h->ws + h->off_scale);
-    a.scale_stride = (long long)(h->st_scale / sizeof(float));
-    a.recv_ids = reinterpret_cast<int32_t *>(h->ws + h->off_ids);
-    a.ids_stride = (long long)(h->st_ids / sizeof(int32_t));
-    a.recv_weights = reinterpret_cast<float *>(h->ws + h->off_weights);
-    a.weights_stride = (long long)(h->st_weights / sizeof(float));
+    // every rank's receive buffers, advanced to the first row of the hosted sources
+    a.row0 = (long long)h->first * T;
+    for (int d = 0; d < h->ep; ++d) {
+        a.recv_hidden[d] = h->t_hidden[d] + a.row0 * h->row_bytes;
+        a.recv_scale[d] = h->t_scale[d] + a.row0 * h->scale_cols;
+        a.recv_ids[d] = h->t_ids[d] + a.row0 * h->top_k;
+        a.recv_weights[d] = h->t_weights[d] + a.row0 * h->top_k;
+    }
     a.route_mask = reinterpret_cast<uint64_t *>(h->ws + h->off_mask);
     a.active = mask;
     a.ep = h->ep;
+    a.src_first = h->first;
+    a.n_src = h->nloc;
     a.num_experts = h->num_experts;
     a.experts_per_rank = h->experts_per_rank;
     a.top_k = h->top_k;
@@ -604,7 +653,9 @@ ep_status ep_dispatch_ex(ep_handle *h, const ep_dispatch_args *args, void *strea
     a.row_bytes = h->row_bytes;
     a.G = hidden_scale ? h->scale_cols : 0;
     a.has_weights = topk_weights ? 1 : 0;
-    a.eplb_dst = h->ws + h->off_eplb;
+    for (int p = 0; p < h->num_parts; ++p)
+        a.eplb_dst[p] = h->t_eplb[p];
+    a.n_eplb_dst = h->num_parts;
     a.eplb_bytes = eplb_bytes;
     a.dev_counts = args->num_tokens_device;
     a.live_counts = args->num_tokens_device ? reinterpret_cast<int32_t *>(h->ws + h->off_counts) : nullptr;
@@ -626,11 +677,13 @@ ep_status ep_dispatch_ex(ep_handle *h, const ep_dispatch_args *args, void *strea
     h->dev_counts = args->num_tokens_device != nullptr;
     h->T = T;
     h->mask = mask;
-    for (int s = 0; s < h->ep; ++s)
+    for (int s = 0; s < h->nloc; ++s)
         h->counts[s] = a.num_tokens[s];
     if (out) {
         out->tokens_per_rank = T;
         out->ep_size = h->ep;
+        out->first_rank = h->first;
+        out->num_ranks = h->nloc;
         out->recv_hidden = h->r_hidden;
         out->recv_scale = hidden_scale ? h->r_scale : nullptr;
         out->recv_topk_ids = h->r_ids;
@@ -649,9 +702,10 @@ ep_status ep_get_combine_input_buffer(ep_handle *h, int rank, void **out)
     *out = nullptr;
     if (!h->pending)
         return fail(EP_ERR_STATE, "the combine input buffer exists only from a dispatch until its combine");
-    if (rank < 0 || rank >= h->ep)
-        return fail(EP_ERR_INVALID_ARG, "rank=%d outside [0, %d)", rank, h->ep);
-    *out = h->ws + h->off_comb + (size_t)rank * h->st_comb;
+    if (rank < h->first || rank >= h->first + h->nloc)
+        return fail(EP_ERR_INVALID_ARG, "rank=%d outside the handle's ranks [%d, %d)", rank, h->first,
+                    h->first + h->nloc);
+    *out = h->ws + h->off_comb + (size_t)(rank - h->first) * h->st_comb;
     return ok();
 }
 
@@ -677,16 +731,19 @@ ep_status ep_combine(ep_handle *h, const void *const *expert_output, void *const
 
     epk::CombineArgs a;
     std::memset(&a, 0, sizeof a);
+    // every rank's combine input, advanced to the first row of the hosted sources
+    a.row0 = (long long)h->first * h->T;
+    const long long row0_bytes = a.row0 * h->hidden * (h->combine_dtype == EP_DTYPE_FP32 ? 4 : 2);
     for (int d = 0; d < h->ep; ++d) {
         const void *p = expert_output ? expert_output[d] : nullptr;
         if (!p)
-            p = h->ws + h->off_comb + (size_t)d * h->st_comb;
+            p = h->t_comb[d];
         else if (!aligned(p, 16))
             return fail(EP_ERR_INVALID_ARG, "expert_output[%d] is not 16-byte aligned", d);
-        a.eo[d] = p;
+        a.eo[d] = static_cast<const uint8_t *>(p) + row0_bytes;
     }
     a.token_offset[0] = 0;
-    for (int s = 0; s < h->ep; ++s) {
+    for (int s = 0; s < h->nloc; ++s) {  // hosted source ranks
         a.num_tokens[s] = h->counts[s];
         a.token_offset[s + 1] = a.token_offset[s] + h->counts[s];
         if (h->counts[s] == 0)
@@ -698,6 +755,8 @@ ep_status ep_combine(ep_handle *h, const void *const *expert_output, void *const
     a.route_mask = reinterpret_cast<const uint64_t *>(h->ws + h->off_mask);
     a.live_counts = h->dev_counts ? reinterpret_cast<const int32_t *>(h->ws + h->off_counts) : nullptr;
     a.ep = h->ep;
+    a.src_first = h->first;
+    a.n_src = h->nloc;
     a.T = h->T;
     a.H = h->hidden;
     a.ctype = (int)h->combine_dtype;
@@ -751,6 +810,131 @@ uint64_t ep_rank_mask(const int *ranks, int n)
 }
 
 const char *ep_last_error(void) { return g_err; }
+
+ep_status ep_partition_describe(const ep_config *cfg, void *workspace, size_t bytes, ep_partition_info *out)
+{
+    if (!out)
+        return fail(EP_ERR_INVALID_ARG, "out is NULL");
+    Layout L{};
+    ep_status st = plan(cfg, &L);
+    if (st != EP_OK)
+        return st;
+    std::memset(out, 0, sizeof *out);
+    out->config = *cfg;
+    out->first_rank = L.first;
+    out->num_ranks = L.nloc;
+    out->workspace = workspace;
+    out->workspace_bytes = bytes;
+    out->off_recv_hidden = L.off_hidden;
+    out->off_recv_scale = L.off_scale;
+    out->off_recv_ids = L.off_ids;
+    out->off_recv_weights = L.off_weights;
+    out->off_combine_in = L.off_comb;
+    out->off_eplb = L.off_eplb;
+    out->stride_recv_hidden = L.st_hidden;
+    out->stride_recv_scale = L.st_scale;
+    out->stride_recv_ids = L.st_ids;
+    out->stride_recv_weights = L.st_weights;
+    out->stride_combine_in = L.st_comb;
+    return ok();
+}
+
+namespace {
+
+// Name of the first field in which two configurations of one group differ
+// (the partition index and the launch flags may differ), or NULL.
+const char *group_config_differs(const ep_config &a, const ep_config &b)
+{
+    const int ga = a.num_partitions <= 1 ? 1 : a.num_partitions;
+    const int gb = b.num_partitions <= 1 ? 1 : b.num_partitions;
+    if (a.ep_size != b.ep_size) return "ep_size";
+    if (a.num_experts != b.num_experts) return "num_experts";
+    if (a.top_k != b.top_k) return "top_k";
+    if (a.hidden != b.hidden) return "hidden";
+    if (a.max_tokens_per_rank != b.max_tokens_per_rank) return "max_tokens_per_rank";
+    if (a.dtype != b.dtype) return "dtype";
+    if ((a.enable_rank_mask != 0) != (b.enable_rank_mask != 0)) return "enable_rank_mask";
+    if (a.scale_cols != b.scale_cols) return "scale_cols";
+    if (a.eplb_stats_max_bytes != b.eplb_stats_max_bytes) return "eplb_stats_max_bytes";
+    if (a.combine_dtype != b.combine_dtype) return "combine_dtype";
+    if (ga != gb) return "num_partitions";
+    return nullptr;
+}
+
+}  // namespace
+
+ep_status ep_partition_check(const ep_partition_info *infos, int n)
+{
+    if (!infos || n < 1 || n > EP_MAX_EP_SIZE)
+        return fail(EP_ERR_INVALID_ARG, "need 1 to %d partition descriptions, got %d", EP_MAX_EP_SIZE, n);
+    const ep_config &c0 = infos[0].config;
+    const int G = c0.num_partitions <= 1 ? 1 : c0.num_partitions;
+    if (n != G)
+        return fail(EP_ERR_INVALID_ARG, "%d descriptions for a group of %d partitions", n, G);
+    for (int p = 0; p < n; ++p) {
+        const ep_partition_info &x = infos[p];
+        if (x.config.partition != p)
+            return fail(EP_ERR_INVALID_ARG, "description %d is of partition %d", p, x.config.partition);
+        if (const char *f = group_config_differs(x.config, c0))
+            return fail(EP_ERR_INVALID_ARG, "partition %d has another %s than partition 0", p, f);
+        Layout L{};
+        if (plan(&x.config, &L) != EP_OK)
+            return EP_ERR_INVALID_ARG;  // message set by plan
+        if (x.first_rank != L.first || x.num_ranks != L.nloc || x.off_recv_hidden != L.off_hidden ||
+            x.off_recv_scale != L.off_scale || x.off_recv_ids != L.off_ids ||
+            x.off_recv_weights != L.off_weights || x.off_combine_in != L.off_comb || x.off_eplb != L.off_eplb ||
+            x.stride_recv_hidden != L.st_hidden || x.stride_recv_scale != L.st_scale ||
+            x.stride_recv_ids != L.st_ids || x.stride_recv_weights != L.st_weights ||
+            x.stride_combine_in != L.st_comb)
+            return fail(EP_ERR_INVALID_ARG, "partition %d: the layout differs from the one its configuration gives", p);
+        if (!x.workspace || !aligned(x.workspace, 256))
+            return fail(EP_ERR_INVALID_ARG, "partition %d: workspace is NULL or not 256-byte aligned", p);
+        if (x.workspace_bytes < L.total)
+            return fail(EP_ERR_INVALID_ARG, "partition %d: workspace has %zu bytes, needs %zu", p,
+                        x.workspace_bytes, L.total);
+        const uintptr_t lo = reinterpret_cast<uintptr_t>(x.workspace), hi = lo + x.workspace_bytes;
+        for (int q = 0; q < p; ++q) {
+            const uintptr_t qlo = reinterpret_cast<uintptr_t>(infos[q].workspace);
+            const uintptr_t qhi = qlo + infos[q].workspace_bytes;
+            if (lo < qhi && qlo < hi)
+                return fail(EP_ERR_INVALID_ARG, "the workspaces of partitions %d and %d overlap", q, p);
+        }
+    }
+    return ok();
+}
+
+ep_status ep_partition_connect(ep_handle *h, const ep_partition_info *infos, int n)
+{
+    if (!h)
+        return fail(EP_ERR_INVALID_ARG, "handle is NULL");
+    if (h->pending)
+        return fail(EP_ERR_STATE, "connect called while a dispatch is pending");
+    ep_status st = ep_partition_check(infos, n);
+    if (st != EP_OK)
+        return st;
+    const ep_partition_info &me = infos[0].config.num_partitions <= 1 ? infos[0] : infos[h->part];
+    if (n != h->num_parts)
+        return fail(EP_ERR_INVALID_ARG, "%d descriptions but the handle is one of %d partitions", n, h->num_parts);
+    if (me.workspace != h->ws)
+        return fail(EP_ERR_INVALID_ARG, "description %d is not of this handle's workspace", h->part);
+    if (const char *f = group_config_differs(me.config, h->cfg))
+        return fail(EP_ERR_INVALID_ARG, "description %d has another %s than the handle", h->part, f);
+    for (int p = 0; p < n; ++p) {
+        const ep_partition_info &x = infos[p];
+        uint8_t *base = static_cast<uint8_t *>(x.workspace);
+        for (int j = 0; j < x.num_ranks; ++j) {
+            const int d = x.first_rank + j;
+            h->t_hidden[d] = base + x.off_recv_hidden + j * x.stride_recv_hidden;
+            h->t_scale[d] = reinterpret_cast<float *>(base + x.off_recv_scale + j * x.stride_recv_scale);
+            h->t_ids[d] = reinterpret_cast<int32_t *>(base + x.off_recv_ids + j * x.stride_recv_ids);
+            h->t_weights[d] = reinterpret_cast<float *>(base + x.off_recv_weights + j * x.stride_recv_weights);
+            h->t_comb[d] = base + x.off_combine_in + j * x.stride_combine_in;
+        }
+        h->t_eplb[p] = base + x.off_eplb;
+    }
+    h->connected = true;
+    return ok();
+}
 
 ep_status ep_binary_version(int *version)
 {

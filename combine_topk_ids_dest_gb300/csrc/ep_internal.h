@@ -70,60 +70,70 @@ static __device__ __noinline__ bool in_bounds(const CheckCtx &c, int site, const
 #endif
 
 // Everything one dispatch launch needs, passed by value as a __grid_constant__
-// kernel parameter (2984 bytes; the combine's block is 1600), so no
+// kernel parameter (about 5 KB; the combine's block is about 1.6 KB), so no
 // host->device copy precedes a launch and the launch can be captured in a
 // CUDA graph as is.
+//
+// A launch handles the source ranks [src_first, src_first + n_src) of an EP
+// group of `ep` ranks (all of them for an unpartitioned handle; one
+// partition's ranks otherwise). Per-source arrays are indexed by the local
+// source i (rank src_first + i); per-destination arrays by the global rank d.
 struct DispatchArgs {
-    const uint8_t *hidden[kMaxEp];  // source rank s: [num_tokens[s], row_bytes]
-    const float *scale[kMaxEp];     // [num_tokens[s], G] or unused
-    const int32_t *ids[kMaxEp];     // [num_tokens[s], K]
-    const float *weights[kMaxEp];   // [num_tokens[s], K] or unused
-    int num_tokens[kMaxEp];         // tokens of rank s; with dev_counts, its maximum
+    const uint8_t *hidden[kMaxEp];  // local source i: [num_tokens[i], row_bytes]
+    const float *scale[kMaxEp];     // [num_tokens[i], G] or unused
+    const int32_t *ids[kMaxEp];     // [num_tokens[i], K]
+    const float *weights[kMaxEp];   // [num_tokens[i], K] or unused
+    int num_tokens[kMaxEp];         // tokens of local source i; with dev_counts, its maximum
 
-    // Device-side counts (NULL: num_tokens is exact): rank s has
-    // clamp(dev_counts[s], 0, num_tokens[s]) tokens; the kernel stores that
-    // into live_counts[s] for the combine.
+    // Device-side counts (NULL: num_tokens is exact): local source i has
+    // clamp(dev_counts[i], 0, num_tokens[i]) tokens; the kernel stores that
+    // into live_counts[i] for the combine.
     const int32_t *dev_counts;
     int32_t *live_counts;
 
-    // Destination rank d's receive buffer of each kind starts at base + d*stride
-    // (strides in elements of the buffer's type); row r = s*T + t.
-    uint8_t *recv_hidden;
-    long long hidden_stride;
-    float *recv_scale;
-    long long scale_stride;
-    int32_t *recv_ids;
-    long long ids_stride;
-    float *recv_weights;
-    long long weights_stride;
+    // Destination rank d's receive buffers, wherever they live (this
+    // handle's workspace or a connected partition's), each of ep*T rows with
+    // row s*T + t for token t of global source rank s. The pointers are
+    // advanced to row row0 = src_first*T, the first row of this launch's
+    // sources, so own slot i*T + t indexes them directly.
+    uint8_t *recv_hidden[kMaxEp];
+    float *recv_scale[kMaxEp];
+    int32_t *recv_ids[kMaxEp];
+    float *recv_weights[kMaxEp];
+    long long row0;
 
-    uint64_t *route_mask;  // [ep*T] destination-rank bit set of each slot
+    uint64_t *route_mask;  // [n_src*T] destination-rank bit set of each own slot i*T + t
     uint64_t active;       // ranks allowed as destinations
 
-    int ep, num_experts, experts_per_rank, top_k, T;
+    int ep, src_first, n_src, num_experts, experts_per_rank, top_k, T;
     int row_bytes;  // hidden row bytes, a multiple of 16
     int G;          // scale columns per row (0 when no scales are sent)
     int has_weights;
 
-    // eplb_local_stats all-gather: rank r's eplb_bytes bytes -> eplb_dst + r*eplb_bytes
+    // eplb_local_stats all-gather: local source i's eplb_bytes bytes -> row
+    // src_first + i of every gathered buffer eplb_dst[p] ([ep][eplb_bytes],
+    // one per partition, n_eplb_dst of them)
     const uint8_t *eplb_src[kMaxEp];
-    uint8_t *eplb_dst;
+    uint8_t *eplb_dst[kMaxEp];
+    int n_eplb_dst;
     int eplb_bytes;  // 0 = nothing to gather; else a multiple of 4
 
     CheckCtx chk;
 };
 
 struct CombineArgs {
-    const void *eo[kMaxEp];  // rank d's combine input, [ep*T, H] of ctype
-    void *out[kMaxEp];       // source rank s's output, [num_tokens[s], H] of ctype
+    const void *eo[kMaxEp];  // global rank d's combine input, [ep*T, H] of ctype, advanced
+                             // to row row0 = src_first*T (own slot i*T + t indexes it)
+    long long row0;
+    void *out[kMaxEp];       // local source i's output, [num_tokens[i], H] of ctype
     int num_tokens[kMaxEp];
-    int token_offset[kMaxEp + 1];  // prefix sums of num_tokens: live token g of rank s has
-                                   // token_offset[s] <= g < token_offset[s+1]
-    const uint64_t *route_mask;    // [ep*T], written by the dispatch
-    const int32_t *live_counts;    // NULL, or [ep] device counts the dispatch stored
+    int token_offset[kMaxEp + 1];  // prefix sums of num_tokens: live token g of local source i
+                                   // has token_offset[i] <= g < token_offset[i+1]
+    const uint64_t *route_mask;    // [n_src*T], written by the dispatch
+    const int32_t *live_counts;    // NULL, or [n_src] device counts the dispatch stored
                                    // (num_tokens are then maxima: rows past the count
                                    // are skipped)
-    int ep, T, H;
+    int ep, src_first, n_src, T, H;
     int ctype;  // element type of eo/out: EP_DTYPE_BF16, EP_DTYPE_FP16 or EP_DTYPE_FP32
 
     CheckCtx chk;

@@ -228,7 +228,10 @@ __global__ void __launch_bounds__(kDispatchThreads)
     constexpr int kVpl = kDispatchVecPerLane * 16 / VB;
     const int lane = threadIdx.x & 31;
     const int wpb = blockDim.x >> 5;
-    const long long n_slots = (long long)a.ep * a.T;
+    const long long n_slots = (long long)a.n_src * a.T;  // this launch's source slots
+#if EP_CHECKED
+    const long long n_rows = (long long)a.ep * a.T;  // rows of every receive buffer (extents)
+#endif
     const long long warp_stride = (long long)gridDim.x * wpb;
     const int K = a.top_k;
     // Nothing below may touch global memory before the previous kernel is done:
@@ -236,19 +239,21 @@ __global__ void __launch_bounds__(kDispatchThreads)
     pdl_launch_dependents();
     pdl_wait();
 
-    // ---- eplb_local_stats all-gather: warp r copies rank r's statistics
-    // into row r of the gathered buffer (a few hundred bytes per rank).
+    // ---- eplb_local_stats all-gather: one warp per (own rank i, gathered
+    // buffer p) copies rank src_first+i's statistics into row src_first+i of
+    // buffer p (a few hundred bytes per rank).
     if (a.eplb_bytes > 0) {
         const long long gw = (long long)blockIdx.x * wpb + (threadIdx.x >> 5);
-        if (gw < a.ep) {
-            const int r = (int)gw;
-            const uint32_t *src = reinterpret_cast<const uint32_t *>(a.eplb_src[r]);
-            uint32_t *dst = reinterpret_cast<uint32_t *>(a.eplb_dst + (long long)r * a.eplb_bytes);
+        if (gw < (long long)a.n_src * a.n_eplb_dst) {
+            const int i = (int)(gw / a.n_eplb_dst);
+            const int p = (int)(gw - (long long)i * a.n_eplb_dst);
+            const uint32_t *src = reinterpret_cast<const uint32_t *>(a.eplb_src[i]);
+            uint32_t *dst = reinterpret_cast<uint32_t *>(a.eplb_dst[p] + (long long)(a.src_first + i) * a.eplb_bytes);
             for (int w = lane; w < (a.eplb_bytes >> 2); w += 32) {
                 uint32_t x = 0;
-                if (EP_IN_BOUNDS(a.chk, kSiteEplbSrc, src + w, 4, a.eplb_src[r], a.eplb_bytes))
+                if (EP_IN_BOUNDS(a.chk, kSiteEplbSrc, src + w, 4, a.eplb_src[i], a.eplb_bytes))
                     x = src[w];
-                if (EP_IN_BOUNDS(a.chk, kSiteEplbDst, dst + w, 4, a.eplb_dst, (long long)a.ep * a.eplb_bytes))
+                if (EP_IN_BOUNDS(a.chk, kSiteEplbDst, dst + w, 4, a.eplb_dst[p], (long long)a.ep * a.eplb_bytes))
                     dst[w] = x;
             }
         }
@@ -265,19 +270,19 @@ __global__ void __launch_bounds__(kDispatchThreads)
     const long long n_items = n_slots * nchunks;
     for (long long item = (long long)blockIdx.x * wpb + (threadIdx.x >> 5); item < n_items;
          item += warp_stride) {
-        const long long slot = item / nchunks;
+        const long long slot = item / nchunks;  // own slot i*T + t
         const int chunk = (int)(item - slot * nchunks);
         const int c0 = chunk * chunk_vecs;
-        const int s = (int)(slot / a.T);
+        const int s = (int)(slot / a.T);  // local source index
         const int t = (int)(slot - (long long)s * a.T);
         int n_s = a.num_tokens[s];
         if (a.dev_counts) {  // counts read at run time, clamped to [0, the host maximum]
             int c = 0;
-            if (EP_IN_BOUNDS(a.chk, kSiteDevCounts, a.dev_counts + s, 4, a.dev_counts, (long long)a.ep * 4))
+            if (EP_IN_BOUNDS(a.chk, kSiteDevCounts, a.dev_counts + s, 4, a.dev_counts, (long long)a.n_src * 4))
                 c = a.dev_counts[s];
             n_s = c < 0 ? 0 : (c < n_s ? c : n_s);
             if (t == 0 && chunk == 0 && lane == 0 &&
-                EP_IN_BOUNDS(a.chk, kSiteLiveCounts, a.live_counts + s, 4, a.live_counts, (long long)a.ep * 4))
+                EP_IN_BOUNDS(a.chk, kSiteLiveCounts, a.live_counts + s, 4, a.live_counts, (long long)a.n_src * 4))
                 a.live_counts[s] = n_s;  // for the combine
         }
         const bool live = t < n_s;
@@ -324,7 +329,6 @@ __global__ void __launch_bounds__(kDispatchThreads)
             a.route_mask[slot] = m;
 
         // ---- id rows of this slot in all destination ranks (first chunk's item)
-        int32_t *ids_slot = a.recv_ids + slot * K;
         if (chunk != 0) {
             // the first chunk's item writes the slot's ids
         } else if ((K & 3) == 0) {
@@ -343,8 +347,8 @@ __global__ void __launch_bounds__(kDispatchThreads)
                     if (!((m >> d) & 1u))
                         v = make_int4(EP_INVALID_EXPERT_ID, EP_INVALID_EXPERT_ID,
                                       EP_INVALID_EXPERT_ID, EP_INVALID_EXPERT_ID);
-                    int32_t *p = ids_slot + d * a.ids_stride + 4 * q;
-                    if (EP_IN_BOUNDS(a.chk, kSiteRecvIds, p, 16, a.recv_ids + d * a.ids_stride, n_slots * K * 4))
+                    int32_t *p = a.recv_ids[d] + slot * K + 4 * q;
+                    if (EP_IN_BOUNDS(a.chk, kSiteRecvIds, p, 16, a.recv_ids[d] - a.row0 * K, n_rows * K * 4))
                         *reinterpret_cast<int4 *>(p) = v;
                 }
             }
@@ -358,8 +362,8 @@ __global__ void __launch_bounds__(kDispatchThreads)
                 if (i < n) {
                     if (!((m >> d) & 1u))
                         v = EP_INVALID_EXPERT_ID;
-                    int32_t *p = ids_slot + d * a.ids_stride + k;
-                    if (EP_IN_BOUNDS(a.chk, kSiteRecvIds, p, 4, a.recv_ids + d * a.ids_stride, n_slots * K * 4))
+                    int32_t *p = a.recv_ids[d] + slot * K + k;
+                    if (EP_IN_BOUNDS(a.chk, kSiteRecvIds, p, 4, a.recv_ids[d] - a.row0 * K, n_rows * K * 4))
                         *p = v;
                 }
             }
@@ -368,15 +372,14 @@ __global__ void __launch_bounds__(kDispatchThreads)
             continue;  // warp-uniform: padding, unrouted or fully masked slot
 
         // ---- this chunk of the hidden row: read once, stored to each routed rank
-        uint8_t *dst_slot = a.recv_hidden + slot * a.row_bytes;
         for (uint64_t mm = m; mm; mm &= mm - 1) {
             const int d = __ffsll((long long)mm) - 1;
-            uint8_t *dst = dst_slot + d * a.hidden_stride;
+            uint8_t *dst = a.recv_hidden[d] + slot * a.row_bytes;
 #pragma unroll
             for (int j = 0; j < kVpl; ++j) {
                 const int idx = c0 + j * 32 + lane;
                 if (idx < nvec && EP_IN_BOUNDS(a.chk, kSiteRecvHidden, dst + VB * (long long)idx, VB,
-                                               a.recv_hidden + d * a.hidden_stride, n_slots * a.row_bytes))
+                                               a.recv_hidden[d] - a.row0 * a.row_bytes, n_rows * a.row_bytes))
                     RV::store(dst + VB * (long long)idx, v[j]);
             }
         }
@@ -386,16 +389,14 @@ __global__ void __launch_bounds__(kDispatchThreads)
         // ---- scale row (G fp32) and weight row (K fp32)
         if (a.G > 0) {
             const float *ssrc = a.scale[s] + (long long)t * a.G;
-            float *sdst = a.recv_scale + slot * a.G;
             for (int j = lane; j < a.G; j += 32) {
                 float x = 0.0f;
                 if (EP_IN_BOUNDS(a.chk, kSiteSrcScale, ssrc + j, 4, a.scale[s], (long long)a.num_tokens[s] * a.G * 4))
                     x = ssrc[j];
                 for (uint64_t mm = m; mm; mm &= mm - 1) {
                     const int d = __ffsll((long long)mm) - 1;
-                    float *p = sdst + d * a.scale_stride + j;
-                    if (EP_IN_BOUNDS(a.chk, kSiteRecvScale, p, 4, a.recv_scale + d * a.scale_stride,
-                                     n_slots * a.G * 4))
+                    float *p = a.recv_scale[d] + slot * a.G + j;
+                    if (EP_IN_BOUNDS(a.chk, kSiteRecvScale, p, 4, a.recv_scale[d] - a.row0 * a.G, n_rows * a.G * 4))
                         *p = x;
                 }
             }
@@ -405,12 +406,10 @@ __global__ void __launch_bounds__(kDispatchThreads)
             float w = 0.0f;
             if (EP_IN_BOUNDS(a.chk, kSiteSrcWeights, wp, 4, a.weights[s], (long long)a.num_tokens[s] * K * 4))
                 w = *wp;
-            float *wdst = a.recv_weights + slot * K + lane;
             for (uint64_t mm = m; mm; mm &= mm - 1) {
                 const int d = __ffsll((long long)mm) - 1;
-                float *p = wdst + d * a.weights_stride;
-                if (EP_IN_BOUNDS(a.chk, kSiteRecvWeights, p, 4, a.recv_weights + d * a.weights_stride,
-                                 n_slots * K * 4))
+                float *p = a.recv_weights[d] + slot * K + lane;
+                if (EP_IN_BOUNDS(a.chk, kSiteRecvWeights, p, 4, a.recv_weights[d] - a.row0 * K, n_rows * K * 4))
                     *p = w;
             }
         }
@@ -449,7 +448,7 @@ __global__ void __launch_bounds__(kCombineMaxThreads)
         // search of the token offsets, so no block is spent on padding slots
         const int g = (int)(b / blocks_per_row);
         const int chunk = (int)(b - (long long)g * blocks_per_row);
-        int lo = 0, hi = a.ep - 1;
+        int lo = 0, hi = a.n_src - 1;
         while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;
             if (a.token_offset[mid] <= g)
@@ -457,23 +456,24 @@ __global__ void __launch_bounds__(kCombineMaxThreads)
             else
                 hi = mid - 1;
         }
-        const int s = lo;
+        const int s = lo;  // local source index
         const int t = g - a.token_offset[s];
         if (a.live_counts) {  // device-side counts: rows past the dispatch's count are skipped
             int c = 0;
-            if (EP_IN_BOUNDS(a.chk, kSiteLiveCounts, a.live_counts + s, 4, a.live_counts, (long long)a.ep * 4))
+            if (EP_IN_BOUNDS(a.chk, kSiteLiveCounts, a.live_counts + s, 4, a.live_counts, (long long)a.n_src * 4))
                 c = a.live_counts[s];
             if (t >= c)
                 continue;
         }
-        const long long slot = (long long)s * a.T + t;
+        const long long slot = (long long)s * a.T + t;  // own slot: routing state
         const int v0 = chunk * (nthr * kV) + threadIdx.x;
         if (v0 >= nvec)
             continue;
         uint64_t m = 0;
-        if (EP_IN_BOUNDS(a.chk, kSiteRouteRead, a.route_mask + slot, 8, a.route_mask, (long long)a.ep * a.T * 8))
+        if (EP_IN_BOUNDS(a.chk, kSiteRouteRead, a.route_mask + slot, 8, a.route_mask, (long long)a.n_src * a.T * 8))
             m = a.route_mask[slot];
-        const long long row = slot * row_bytes;  // byte offset of the slot's row in a rank's buffer
+        // byte offset of the token's row from eo[d], which points at row row0 = src_first*T
+        const long long row = slot * row_bytes;
 
         float acc[kV][kH][kEpv];
 #pragma unroll
@@ -504,7 +504,8 @@ __global__ void __launch_bounds__(kCombineMaxThreads)
 #pragma unroll
                     for (int j = 0; j < kV; ++j) {
                         const int v = v0 + j * nthr;
-                        if (v < nvec && EP_IN_BOUNDS(a.chk, kSiteCombineIn, base + VB * (long long)v, VB, a.eo[d],
+                        if (v < nvec && EP_IN_BOUNDS(a.chk, kSiteCombineIn, base + VB * (long long)v, VB,
+                                                     static_cast<const uint8_t *>(a.eo[d]) - a.row0 * row_bytes,
                                                      (long long)a.ep * a.T * row_bytes))
                             x[r][j] = RV::load(base + VB * (long long)v);
                     }
@@ -622,14 +623,17 @@ cudaError_t kernel_binary_versions(int *out, int max, int *n)
 
 cudaError_t launch_dispatch(const DispatchArgs &a, cudaStream_t stream, bool pdl)
 {
-    const long long n_slots = (long long)a.ep * a.T;
+    const long long n_slots = (long long)a.n_src * a.T;
     if (n_slots == 0 && a.eplb_bytes == 0)
         return cudaSuccess;
     // 32-byte accesses need every source row and receive row 32-byte aligned:
-    // row_bytes % 32 == 0 (receive regions are 256-byte aligned) and every
-    // source base pointer of a rank with tokens.
-    bool wide = EP_DISPATCH_WIDE && (a.row_bytes % 32 == 0) && (a.hidden_stride % 32 == 0);
-    for (int s = 0; wide && s < a.ep; ++s)
+    // row_bytes % 32 == 0, every receive buffer and every source base pointer
+    // of a rank with tokens.
+    bool wide = EP_DISPATCH_WIDE && (a.row_bytes % 32 == 0);
+    for (int d = 0; wide && d < a.ep; ++d)
+        if ((reinterpret_cast<uintptr_t>(a.recv_hidden[d]) % 32) != 0)
+            wide = false;
+    for (int s = 0; wide && s < a.n_src; ++s)
         if (a.num_tokens[s] > 0 && (reinterpret_cast<uintptr_t>(a.hidden[s]) % 32) != 0)
             wide = false;
     const int wpb = kDispatchThreads / 32;
@@ -639,7 +643,8 @@ cudaError_t launch_dispatch(const DispatchArgs &a, cudaStream_t stream, bool pdl
     const long long cap = (long long)sm_count() * kDispatchBlocksPerSm;
     if (blocks > cap)
         blocks = cap;
-    const long long eplb_blocks = a.eplb_bytes > 0 ? (a.ep + wpb - 1) / wpb : 0;  // one warp per rank
+    // one warp per (own rank, gathered buffer)
+    const long long eplb_blocks = a.eplb_bytes > 0 ? ((long long)a.n_src * a.n_eplb_dst + wpb - 1) / wpb : 0;
     if (blocks < eplb_blocks)
         blocks = eplb_blocks;
     cudaError_t ce = wide ? launch(dispatch_kernel<32>, blocks, kDispatchThreads, stream, pdl, a)
@@ -654,7 +659,7 @@ cudaError_t launch_combine(const CombineArgs &a, cudaStream_t stream, bool pdl)
     const int threads = combine_threads(nvec);
     const int per_block = threads * kCombineVpt;
     const int bpr = (nvec + per_block - 1) / per_block;
-    const long long n_blocks = (long long)a.token_offset[a.ep] * bpr;
+    const long long n_blocks = (long long)a.token_offset[a.n_src] * bpr;
     if (n_blocks == 0)
         return cudaSuccess;
     long long grid = n_blocks;
@@ -665,12 +670,12 @@ cudaError_t launch_combine(const CombineArgs &a, cudaStream_t stream, bool pdl)
     // (measured on GB300: ~7.2 vs ~7.0 TB/s incremental, ~17 vs ~11 us fixed;
     // equal at ~117 MB of output, faster from ~235 MB), so they are used only
     // for large combines: output of at least 192 MiB.
-    const long long out_bytes = (long long)a.token_offset[a.ep] * a.H * elem;
+    const long long out_bytes = (long long)a.token_offset[a.n_src] * a.H * elem;
     bool wide = EP_COMBINE_WIDE && (((long long)a.H * elem) % 32 == 0) && out_bytes >= (192LL << 20);
     for (int d = 0; wide && d < a.ep; ++d)
         if ((reinterpret_cast<uintptr_t>(a.eo[d]) % 32) != 0)
             wide = false;
-    for (int s = 0; wide && s < a.ep; ++s)
+    for (int s = 0; wide && s < a.n_src; ++s)
         if (a.num_tokens[s] > 0 && (reinterpret_cast<uintptr_t>(a.out[s]) % 32) != 0)
             wide = false;
 #define EP_LAUNCH_COMBINE(CT)                                                          \

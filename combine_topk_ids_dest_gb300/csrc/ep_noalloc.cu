@@ -195,6 +195,9 @@ extern "C" ep_status ep_combine_noalloc(int ep_size, int num_experts, int top_k,
     a.T = tokens_per_rank;
     c.route_mask = route;
     c.ep = ep_size;
+    c.row0 = 0;
+    c.src_first = 0;
+    c.n_src = ep_size;
     c.T = tokens_per_rank;
     c.H = hidden;
     c.ctype = EP_DTYPE_BF16;

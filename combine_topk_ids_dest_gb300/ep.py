@@ -6,7 +6,8 @@ interface (pages "flashinfer.moe_ep.MoEEpCommunication" and
 ``dispatch``, ``combine``, ``get_combine_input_buffer``, ``active_rank_mask``,
 ``destroy``) for an EP group whose ``ep_size`` ranks are virtual ranks on one
 GPU. Every per-rank argument is a list with one tensor per rank; every
-result is a list with one tensor per rank. All work runs in the CUDA library
+result is a list with one tensor per rank (per rank of the communicator's
+partition, for a partitioned group). All work runs in the CUDA library
 on torch's current stream; torch supplies device memory and streams only.
 """
 from __future__ import annotations
@@ -91,6 +92,14 @@ class EpComm:
     workspace is allocated here with torch, at capacity
     ``max_tokens_per_rank``.
 
+    ``num_partitions`` G > 1 makes this communicator partition ``partition``
+    of a partitioned group: it hosts ranks ``first_rank ..
+    first_rank+num_ranks-1`` (``num_ranks = ep_size // G``) in a workspace of
+    its own, takes per-rank arguments for those ranks only (entry j is rank
+    first_rank + j) and must be connected with every partition of the group
+    (``connect`` / ``connect_partitions``) before its first dispatch. Its
+    combine reads every rank's combine input, wherever it lives.
+
     Different communicators may be used from different threads at once; one
     communicator must not (it holds the state of its pending dispatch).
     """
@@ -99,7 +108,7 @@ class EpComm:
                  max_tokens_per_rank: int, dtype: torch.dtype = torch.bfloat16,
                  enable_rank_mask: bool = False, device=None, scale_cols: Optional[int] = None,
                  eplb_stats_max_bytes: int = 0, combine_dtype: torch.dtype = torch.bfloat16,
-                 pdl: bool = False):
+                 pdl: bool = False, num_partitions: int = 1, partition: int = 0):
         self._L = _lib.load()
         if dtype not in _DTYPES:
             raise ValueError(f"dtype {dtype} not supported (bfloat16, float8_e4m3fn, float16, float32)")
@@ -117,10 +126,16 @@ class EpComm:
             raise ValueError(f"combine_dtype {combine_dtype} not supported (bfloat16, float16, float32)")
         self.combine_dtype = combine_dtype
         self.pdl = bool(pdl)
+        self.num_partitions, self.partition = max(1, int(num_partitions)), int(partition)
+        if self.ep_size % self.num_partitions or not 0 <= self.partition < self.num_partitions:
+            raise ValueError(f"partition {partition} of {num_partitions} does not split ep_size={ep_size}")
+        self.num_ranks = self.ep_size // self.num_partitions
+        self.first_rank = self.partition * self.num_ranks
         cfg = _lib.EpConfigC(self.ep_size, self.num_experts, self.top_k, self.hidden,
                              self.max_tokens_per_rank, _DTYPES[dtype], int(self.enable_rank_mask),
                              self.scale_cols, self.eplb_stats_max_bytes, _DTYPES[combine_dtype],
-                             _lib.EP_LAUNCH_PDL if self.pdl else 0)
+                             _lib.EP_LAUNCH_PDL if self.pdl else 0, self.num_partitions, self.partition)
+        self._cfg = cfg
         nbytes = ctypes.c_size_t(0)
         check(self._L.ep_workspace_size_ex(ctypes.byref(cfg), ctypes.byref(nbytes)))
         with torch.cuda.device(self.device):
@@ -171,10 +186,26 @@ class EpComm:
             raise ValueError(f"{name}[{s}] must be a contiguous [{n}, {cols}] tensor, got "
                              f"{tuple(t.shape)}")
 
+    # -- partitioned groups (C ABI ep_partition_*) ----------------------------
+    def partition_info(self) -> "_lib.EpPartitionInfoC":
+        """This communicator's partition as its peers see it (ep_partition_describe)."""
+        self._live()
+        info = _lib.EpPartitionInfoC()
+        check(self._L.ep_partition_describe(ctypes.byref(self._cfg), ctypes.c_void_p(self._ws.data_ptr()),
+                                            self._ws.numel(), ctypes.byref(info)))
+        return info
+
+    def connect(self, infos: Sequence["_lib.EpPartitionInfoC"]) -> None:
+        """Connect with every partition of the group (``infos`` in partition
+        order, this one's included): ep_partition_connect."""
+        self._live()
+        arr = (_lib.EpPartitionInfoC * len(infos))(*infos)
+        check(self._L.ep_partition_connect(self._h, arr, len(infos)))
+
     def _check_stacked(self, name, t, M, cols, dtype):
-        """Checks one stacked operand, [ep_size, M, cols] (M from the tensor when
+        """Checks one stacked operand, [num_ranks, M, cols] (M from the tensor when
         None); returns M."""
-        ep = self.ep_size
+        ep = self.num_ranks
         if not isinstance(t, torch.Tensor) or t.dim() != 3 or t.shape[0] != ep or t.shape[2] != cols \
                 or (M is not None and t.shape[1] != M):
             want = f"[{ep}, {'M' if M is None else M}, {cols}]"
@@ -195,7 +226,7 @@ class EpComm:
         v = self._views.get(key)
         if v is None:
             rows = self.ep_size * T
-            v = [self._view(ptrs[d], rows, cols, dtype) for d in range(self.ep_size)]
+            v = [self._view(ptrs[j], rows, cols, dtype) for j in range(self.num_ranks)]
             self._views[key] = v
         return list(v)
 
@@ -233,7 +264,7 @@ class EpComm:
         the first count rows of each output.
         """
         self._live()
-        ep, K, H = self.ep_size, self.top_k, self.hidden
+        ep, K, H = self.num_ranks, self.top_k, self.hidden  # ep: source ranks of this communicator
         G = self.scale_cols
         stacked = isinstance(hidden_states, torch.Tensor)
         if stacked:
@@ -320,21 +351,22 @@ class EpComm:
             if res.recv_topk_weights else None
         stats = None
         if eplb_meta is not None:
+            n = self.ep_size  # every rank's statistics, this partition's and its peers'
             off = int(res.eplb_global_stats) - self._ws.data_ptr()
-            stats = self._ws[off:off + ep * eplb_bytes].view(eplb_meta[0]).view((ep,) + eplb_meta[1])
+            stats = self._ws[off:off + n * eplb_bytes].view(eplb_meta[0]).view((n,) + eplb_meta[1])
         return EpDispatchResult(T, hs, sc, ids, w, stats)
 
     # -- MoEEpCommunication.get_combine_input_buffer ------------------------
     def get_combine_input_buffer(self, dtype: Optional[torch.dtype] = None, *,
                                  rank: Optional[int] = None):
         """Rank ``rank``'s [ep_size*tokens_per_rank, hidden] combine input of
-        the communicator's combine dtype (all ranks as a list when ``rank`` is
-        None); None when ``dtype`` names another type (no such buffer).
-        Usable from a dispatch() until the combine() that follows it."""
+        the communicator's combine dtype (all of its ranks as a list when
+        ``rank`` is None); None when ``dtype`` names another type (no such
+        buffer). Usable from a dispatch() until the combine() that follows it."""
         self._live()
         if dtype is not None and dtype != self.combine_dtype:
             return None
-        ranks = range(self.ep_size) if rank is None else [int(rank)]
+        ranks = range(self.first_rank, self.first_rank + self.num_ranks) if rank is None else [int(rank)]
         out = []
         for r in ranks:
             p = ctypes.c_void_p()
@@ -365,6 +397,7 @@ class EpComm:
         n_s rows; the rows past them are not written)."""
         self._live()
         ep, H = self.ep_size, self.hidden
+        nr = self.num_ranks  # source ranks of this communicator (outputs)
         if self._counts is None:
             raise EpError(_lib.EP_ERR_STATE, "combine called without a pending dispatch")
         rows = ep * self._T
@@ -391,23 +424,23 @@ class EpComm:
                 eo_ptrs.append(e.data_ptr())
             eo_ptrs = _addr_array(eo_ptrs)
         if output is None and self._stacked:
-            output = torch.empty(ep, max(self._counts, default=0), H, dtype=self.combine_dtype,
+            output = torch.empty(nr, max(self._counts, default=0), H, dtype=self.combine_dtype,
                                  device=self.device)
         if isinstance(output, torch.Tensor):
             o = output
-            if o.dim() != 3 or o.shape[0] != ep or o.shape[2] != H or o.shape[1] < max(self._counts, default=0) \
+            if o.dim() != 3 or o.shape[0] != nr or o.shape[2] != H or o.shape[1] < max(self._counts, default=0) \
                     or o.dtype is not self.combine_dtype or not o.is_cuda or o.get_device() != self._dev_index \
                     or not o.is_contiguous():
-                raise ValueError(f"a stacked output must be a contiguous {self.combine_dtype} [{ep}, M, {H}] "
+                raise ValueError(f"a stacked output must be a contiguous {self.combine_dtype} [{nr}, M, {H}] "
                                  f"tensor on {self.device} with M >= {max(self._counts, default=0)}")
             out_ptrs = self._stacked_ptrs(o, int(o.shape[1]), H)
         else:
             if output is None:
                 output = [torch.empty(n, H, dtype=self.combine_dtype, device=self.device) for n in self._counts]
             else:
-                if len(output) != ep:
-                    raise ValueError(f"output needs {ep} per-rank tensors")
-                for s in range(ep):
+                if len(output) != nr:
+                    raise ValueError(f"output needs {nr} per-rank tensors")
+                for s in range(nr):
                     self._check_rank_tensor("output", output[s], s, self._counts[s], H, self.combine_dtype)
             out_ptrs = _addr_array([o.data_ptr() for o in output])
         with torch.cuda.device(self.device):
@@ -440,6 +473,31 @@ class EpComm:
                 self._h = None
         except Exception:
             pass
+
+
+def connect_partitions(comms: Sequence[EpComm]) -> None:
+    """Connects the communicators of every partition of one group, all in
+    this process (``comms[p]`` is partition p)."""
+    infos = [c.partition_info() for c in comms]
+    for c in comms:
+        c.connect(infos)
+
+
+def gather_partition_infos(info: "_lib.EpPartitionInfoC", group=None) -> List["_lib.EpPartitionInfoC"]:
+    """All partitions' descriptions, in partition order, from one process per
+    partition of a torch.distributed group: each process passes its own
+    (``EpComm.partition_info()``, its workspace address replaced by one its
+    peers can use). The result is checked with ep_partition_check, so every
+    process learns of a mismatch in the group's configuration."""
+    import torch.distributed as dist
+    world = dist.get_world_size(group)
+    gathered = [None] * world
+    dist.all_gather_object(gathered, bytes(info), group=group)
+    infos = sorted((_lib.EpPartitionInfoC.from_buffer_copy(b) for b in gathered),
+                   key=lambda x: x.config.partition)
+    arr = (_lib.EpPartitionInfoC * len(infos))(*infos)
+    check(_lib.load().ep_partition_check(arr, len(infos)))
+    return infos
 
 
 def combine_noalloc(num_experts: int, top_k: int, topk_ids: Sequence[torch.Tensor],

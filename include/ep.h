@@ -96,13 +96,16 @@ typedef enum {
 typedef struct ep_handle ep_handle;
 
 /* Where one dispatch left its results. All arrays are host arrays owned by
- * the handle, each with ep_size device pointers (entry d = destination rank
- * d). Buffer d holds ep_size*tokens_per_rank rows; row s*tokens_per_rank+t
- * is token t of source rank s. The pointers stay valid until ep_destroy; the
- * contents until the next ep_dispatch. */
+ * the handle, each with one device pointer per rank of the handle (entry j =
+ * destination rank first_rank + j; every rank unless the handle is a
+ * partition). Each buffer holds ep_size*tokens_per_rank rows; row
+ * s*tokens_per_rank+t is token t of source rank s. The pointers stay valid
+ * until ep_destroy; the contents until the next ep_dispatch. */
 typedef struct {
     int tokens_per_rank;
     int ep_size;
+    int first_rank;                   /* the arrays' entry j is rank first_rank + j ... */
+    int num_ranks;                    /* ... for j < num_ranks (0 and ep_size unless partitioned) */
     void *const *recv_hidden;         /* rows of `hidden` elements of the payload dtype */
     float *const *recv_scale;         /* rows of scale_cols fp32, or NULL if none were sent */
     int32_t *const *recv_topk_ids;    /* rows of top_k int32 */
@@ -132,6 +135,9 @@ typedef struct {
                                   EP_DTYPE_BF16 (0, the default), EP_DTYPE_FP16 or EP_DTYPE_FP32;
                                   hidden*elem_bytes of it must be a multiple of 16 */
     int launch_flags;          /* 0 or EP_LAUNCH_PDL (below) */
+    int num_partitions;        /* 0 or 1: one handle holds every rank. G > 1 (dividing ep_size):
+                                  the handle is one partition of the group (below) */
+    int partition;             /* which partition, 0 <= partition < num_partitions */
 } ep_config;
 
 /* ep_config.launch_flags bit: launch the dispatch and combine kernels with
@@ -154,8 +160,12 @@ typedef struct {
  * device pointer to rank r's eplb_stats_bytes bytes of expert-load
  * statistics (4-byte aligned; every rank passes the same size), gathered
  * into ep_dispatch_result.eplb_global_stats by the same launch
- * (MoEEpCommunication.dispatch, parameter eplb_local_stats).
- * num_tokens_device: NULL, or a device int32 [ep_size] array the kernels
+ * (MoEEpCommunication.dispatch, parameter eplb_local_stats). A partition
+ * handle writes its ranks' rows into every partition's gathered buffer, so
+ * each holds all ranks' rows once every partition has dispatched (all pass
+ * the same eplb_stats_bytes).
+ * num_tokens_device: NULL, or a device int32 [ep_size] array (one entry per
+ * hosted rank for a partition handle) the kernels
  * read when they run: rank s then has min(max(num_tokens_device[s], 0),
  * num_tokens[s]) tokens, and num_tokens (host) gives each rank's maximum
  * (its source tensors hold that many rows). This lets one captured CUDA
@@ -220,7 +230,9 @@ ep_status ep_create_with_workspace(int ep_size, int num_experts, int top_k, int 
 ep_status ep_create_ex(const ep_config *cfg, void *workspace, size_t bytes, ep_handle **out);
 
 /* Dispatch of all ep_size source ranks (MoEEpCommunication.dispatch;
- * NVLinkOneSidedAlltoAll.dispatch for active_rank_mask).
+ * NVLinkOneSidedAlltoAll.dispatch for active_rank_mask). For a partition
+ * handle: of the ranks it hosts, and every per-rank array below has one
+ * entry per hosted rank (see "Partitioned EP groups").
  *  hidden[s]       device [num_tokens[s], hidden] payload dtype, 16-byte aligned
  *  hidden_scale    NULL, or hidden_scale[s] device fp32 [num_tokens[s], scale_cols]
  *                  (scale_cols = hidden/128 for ep_create handles; needs scale_cols > 0)
@@ -299,6 +311,71 @@ const char *ep_last_error(void);
  * kernels report different versions. Runs no kernel. (Not on the pages: a
  * build check.) */
 ep_status ep_binary_version(int *version);
+
+/* ---- Partitioned EP groups -------------------------------------------------
+ * The pages' backends (NVLinkOneSidedAlltoAll, class description) run one
+ * rank per GPU and move rows between the GPUs' buffers with one-sided
+ * stores and loads. A partitioned group is that layout for virtual ranks:
+ * the ep_size ranks are split into G = num_partitions contiguous blocks of
+ * ep_size/G ranks; partition g hosts ranks [g*ep_size/G, (g+1)*ep_size/G)
+ * in a workspace of its own (its ranks' receive and combine-input buffers,
+ * the routing state of its own source tokens) and has a handle of its own.
+ * Its dispatch scatters its own ranks' tokens into the receive rows of every
+ * rank, in whichever partition's workspace those live, through a table of
+ * destination addresses; its combine sums its own tokens' rows from every
+ * rank's combine input, in ascending rank order, exactly as the unpartitioned
+ * combine does. Results are bit for bit those of one handle over all ranks.
+ *
+ * Per-rank arguments of a partition handle have one entry per rank it hosts
+ * (entry j = rank first_rank + j): ep_dispatch's hidden, hidden_scale,
+ * topk_ids, topk_weights, num_tokens (and ep_dispatch_args'
+ * eplb_local_stats and num_tokens_device), and ep_combine's output.
+ * ep_combine's expert_output keeps ep_size entries (every rank's rows are
+ * read); ep_get_combine_input_buffer takes a rank the partition hosts.
+ *
+ * Set-up: each partition describes itself (ep_partition_describe: its
+ * configuration and the layout of its workspace), the descriptions of all
+ * G partitions are brought together, and every handle is connected with all
+ * of them (ep_partition_connect), which checks that they form one group. An
+ * address in a description must be valid on the device of the handle that
+ * is connected with it; on one GPU the workspaces are simply separate
+ * allocations. Every partition dispatches once per step with the same
+ * runtime_max_tokens_per_rank and mask; a partition's receive buffers are
+ * complete once every partition's dispatch has completed, and a combine may
+ * start only after every rank's expert outputs are written: ordering across
+ * partitions is the caller's (stream order, or events between streams). */
+
+/* One partition as its peers see it. */
+typedef struct {
+    ep_config config;           /* the partition's configuration */
+    int first_rank, num_ranks;  /* the ranks it hosts */
+    void *workspace;            /* device address of its workspace */
+    size_t workspace_bytes;     /* its size (at least ep_workspace_size_ex) */
+    /* byte offsets of its regions in the workspace, and bytes per hosted rank
+     * (receive hidden/scale/ids/weights, combine input); the eplb buffer */
+    size_t off_recv_hidden, off_recv_scale, off_recv_ids, off_recv_weights, off_combine_in, off_eplb;
+    size_t stride_recv_hidden, stride_recv_scale, stride_recv_ids, stride_recv_weights, stride_combine_in;
+} ep_partition_info;
+
+/* Fills *out for the partition cfg->partition of a group configured by
+ * `cfg`, whose workspace is `workspace` (bytes as given). Host only; needs
+ * no GPU. EP_ERR_INVALID_ARG on a bad configuration. */
+ep_status ep_partition_describe(const ep_config *cfg, void *workspace, size_t bytes, ep_partition_info *out);
+
+/* Checks that infos[0..n) describe one partitioned group: n ==
+ * num_partitions, infos[p] is partition p, all configurations equal but for
+ * `partition`, each layout is the one its configuration gives, workspaces
+ * are large enough, 256-byte aligned and do not overlap. Host only;
+ * EP_ERR_INVALID_ARG with the first problem in ep_last_error otherwise. */
+ep_status ep_partition_check(const ep_partition_info *infos, int n);
+
+/* Connects a partition handle with all partitions of its group (its own
+ * description included, which must match the handle): ep_partition_check,
+ * then the handle's destination tables are filled. Required once before the
+ * first dispatch of a partition handle (EP_ERR_STATE otherwise); may be
+ * repeated while no dispatch is pending. An unpartitioned handle needs no
+ * connection (connecting it with its own description is accepted). */
+ep_status ep_partition_connect(ep_handle *h, const ep_partition_info *infos, int n);
 
 /* Largest ep_size * tokens_per_rank that ep_combine_noalloc accepts. */
 #define EP_NOALLOC_MAX_SLOTS 65536

@@ -129,7 +129,8 @@ def test_create_without_gpu_reports_error():
 
 def _size_ex(**kw):
     base = dict(ep_size=4, num_experts=8, top_k=2, hidden=256, max_tokens_per_rank=16, dtype=0,
-                enable_rank_mask=0, scale_cols=-1, eplb_stats_max_bytes=0, combine_dtype=0, launch_flags=0)
+                enable_rank_mask=0, scale_cols=-1, eplb_stats_max_bytes=0, combine_dtype=0, launch_flags=0,
+                num_partitions=0, partition=0)
     base.update(kw)
     cfg = _lib.EpConfigC(*[base[f] for f, _ in _lib.EpConfigC._fields_])
     n = ctypes.c_size_t(0)

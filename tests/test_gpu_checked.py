@@ -3,7 +3,8 @@ access of the kernels is tested against the extent of its buffer; an access
 outside is skipped and the call returns EP_ERR_DEVICE_CHECK.
 
 test_gpu_suite_under_checked_build runs the parity, golden, eplb, fuzz,
-graph, stream, device-count, stacked-form, full-size and no-alloc GPU tests in a child process that loads the
+graph, stream, device-count, stacked-form, full-size, programmatic-launch,
+partitioned-group and no-alloc GPU tests in a child process that loads the
 checked library. Every call there waits for its kernels and reads the check
 record, so the suite passing shows that none of those runs touched memory
 outside the buffers the C ABI gives each operand; the full-size workloads
@@ -33,7 +34,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SUITE = ["tests/test_gpu_parity.py", "tests/test_gpu_golden.py", "tests/test_gpu_eplb.py",
          "tests/test_gpu_fuzz.py", "tests/test_gpu_graph.py", "tests/test_gpu_streams.py",
          "tests/test_gpu_checked.py", "tests/test_gpu_device_counts.py", "tests/test_gpu_stacked.py",
-         "tests/test_gpu_fullsize.py", "tests/test_zz_no_alloc.py"]
+         "tests/test_gpu_fullsize.py", "tests/test_gpu_pdl.py", "tests/test_gpu_partitions.py",
+         "tests/test_zz_no_alloc.py"]
 
 in_checked_child = pytest.mark.skipif(not _lib.checked(), reason="runs in the checked build's child process")
 
