@@ -396,16 +396,56 @@ def whole_job_gbs(bytes_per_round: int, rounds: int, world: int, max_total_ms: f
 # ---------------------------------------------------------------------------
 # CPU oracle leg
 # ---------------------------------------------------------------------------
-def _sample_inputs(inp, m: int):
-    """The first min(m, n_s) tokens of every source rank, as a workload with
-    tokens_per_rank m (the oracle's bounded sample of the full workload)."""
+def _sample_inputs(inp, m: int, t0: int = 0):
+    """Tokens [t0, t0+m) of every source rank (as many as it has), as a
+    workload with tokens_per_rank m: the oracle's bounded sample of the full
+    workload. Under the rank-major row rule such a slice of tokens is a
+    problem of its own (its row s*m+j stands for full row s*T+t0+j)."""
     wl = inp.wl
-    counts = [min(m, n) for n in inp.num_tokens]
-    sub = lambda lst: None if lst is None else [x[:c] for x, c in zip(lst, counts)]
+    counts = [max(0, min(m, n - t0)) for n in inp.num_tokens]
+    # copies, not views: a view would carry (and pickle) its whole storage
+    sub = lambda lst: None if lst is None else [x[t0:t0 + c].clone() for x, c in zip(lst, counts)]
     swl = wl.replace(capacity=m, runtime_max=None, counts=("fixed",) + tuple(counts))
     return workloads.EpInputs(wl=swl, num_tokens=counts, hidden=sub(inp.hidden), scale=sub(inp.scale),
                               topk_ids=sub(inp.topk_ids), topk_weights=sub(inp.topk_weights),
                               active_rank_mask=inp.active_rank_mask)
+
+
+def _oracle_chunk_timed(s):
+    """Runs in a worker process: one chunk's oracle round, timed by the wall
+    clock the parent shares; returns (start, end, algorithmic bytes)."""
+    import numpy as np
+    torch.set_num_threads(1)  # one core per process: torch's own thread pool would oversubscribe them
+    wl = s.wl
+    rows = torch.arange(wl.ep_size * wl.tokens_per_rank)
+    eo = [workloads.expert_output_rows(1, d, rows, wl.hidden).view(torch.int16).numpy().view(np.uint16)
+          for d in range(wl.ep_size)]
+    t0 = time.time()
+    _oracle_round(s, eo)
+    return t0, time.time(), round_bytes(s)["total"]
+
+
+def oracle_parallel(inp, seconds: float, m_single: int):
+    """The unchanged single-threaded oracle on every host core at once: one
+    spawn-started process per core, each on its own chunk of tokens (tokens
+    [w*m, (w+1)*m) of every rank, m chosen so a chunk takes about `seconds`,
+    at most the workload split evenly). GB/s = all chunks' bytes over the
+    wall time from the first chunk's start to the last one's end."""
+    import concurrent.futures as cf
+    import multiprocessing as mp
+    n = len(os.sched_getaffinity(0))
+    T = inp.wl.tokens_per_rank
+    m = max(1, min(m_single, -(-T // n)))
+    chunks = [_sample_inputs(inp, m, w * m) for w in range(n) if w * m < max(inp.num_tokens)]
+    with cf.ProcessPoolExecutor(max_workers=len(chunks), mp_context=mp.get_context("spawn")) as ex:
+        list(ex.map(_oracle_chunk_timed, [_sample_inputs(inp, 1)] * len(chunks)))  # start and warm every worker
+        res = list(ex.map(_oracle_chunk_timed, chunks))
+    wall = max(r[1] for r in res) - min(r[0] for r in res)
+    nbytes = sum(r[2] for r in res)
+    desc = (f"{len(chunks)} processes at once, each the single-threaded C oracle on {m} tokens of every "
+            f"source rank (tokens [w*{m}, (w+1)*{m}) in process w; {sum(sum(c.num_tokens) for c in chunks)} of "
+            f"{inp.total_tokens} tokens)")
+    return nbytes / wall / 1e9, len(chunks), desc, wall
 
 
 def _oracle_round(s, eo):
@@ -446,7 +486,7 @@ def oracle_sample(inp, seconds: float):
     b = round_bytes(s)
     desc = (f"first {m} of {T} tokens per source rank ({s.total_tokens} of {inp.total_tokens} tokens), "
             f"all {wl.ep_size} ranks, same ids/masks/payload; single-threaded C oracle")
-    return s, eo, b, desc
+    return s, eo, b, desc, m
 
 
 def run_reference(args, rank, world):
@@ -459,7 +499,7 @@ def run_reference(args, rank, world):
     # the whole arm takes about --reference-seconds for any step count (the
     # oracle's cost grows linearly with the sample, so GB/s does not depend on it)
     per_step = max(0.05, args.reference_seconds / max(1, args.steps + args.warmup))
-    s, eo, b, desc = oracle_sample(inp, per_step)
+    s, eo, b, desc, _ = oracle_sample(inp, per_step)
     for _ in range(args.warmup):
         _oracle_round(s, eo)
     times = []
@@ -646,7 +686,7 @@ def run_ours(args, rank, world):
         "clocks": clocks.summary(),
     }
     if world == 1 and not args.no_cpu_baseline:
-        s, eo, sb, desc = oracle_sample(inp, args.cpu_seconds)
+        s, eo, sb, desc, m = oracle_sample(inp, args.cpu_seconds)
         t0 = time.perf_counter()
         _oracle_round(s, eo)
         dt = time.perf_counter() - t0
@@ -655,6 +695,11 @@ def run_ours(args, rank, world):
                                 "sample": desc, "seconds": dt,
                                 "us_per_round_extrapolated": 1e6 * b["total"] / (cpu_gbs * 1e9),
                                 "host_cores_available": len(os.sched_getaffinity(0))}
+        if len(os.sched_getaffinity(0)) > 1:
+            pgbs, cores, pdesc, wall = oracle_parallel(inp, args.cpu_seconds, m)
+            line["cpu_baseline_all_cores"] = {
+                "value": pgbs, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": pdesc,
+                "seconds": wall, "us_per_round_extrapolated": 1e6 * b["total"] / (pgbs * 1e9)}
     print(json.dumps(line), flush=True)
 
 

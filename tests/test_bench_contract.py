@@ -141,3 +141,25 @@ def test_quantile():
     assert bench._quantile([3, 1, 2, 5, 4], 0.5) == 3
     assert abs(bench._quantile([1, 2, 3, 4, 5], 0.1) - 1.4) < 1e-12
     assert bench._quantile([7], 0.9) == 7
+
+
+def test_all_cores_oracle_leg_covers_distinct_token_slices():
+    """The all-cores CPU baseline runs the unchanged oracle in one process per
+    core, each on its own slice of tokens of every rank; the slices are
+    disjoint and their bytes add up to the bytes of the tokens they cover."""
+    import bench
+    wl = workloads.WORKLOADS["tiny"]
+    inp = workloads.make_inputs(wl)
+    gbs, procs, desc, wall = bench.oracle_parallel(inp, 0.1, 4)
+    assert gbs > 0 and wall > 0 and 1 <= procs <= len(os.sched_getaffinity(0))
+    m = max(1, min(4, -(-wl.tokens_per_rank // len(os.sched_getaffinity(0)))))
+    chunks = [bench._sample_inputs(inp, m, w * m) for w in range(procs)]
+    assert sum(sum(c.num_tokens) for c in chunks) <= inp.total_tokens
+    assert f"{procs} processes" in desc
+    import torch
+    for w, c in enumerate(chunks):  # slice w holds rows [w*m, w*m + count) of the full inputs
+        for s in range(wl.ep_size):
+            n = c.num_tokens[s]
+            assert n == max(0, min(m, inp.num_tokens[s] - w * m))
+            assert torch.equal(c.topk_ids[s], inp.topk_ids[s][w * m:w * m + n])
+            assert torch.equal(c.hidden[s], inp.hidden[s][w * m:w * m + n])
