@@ -66,12 +66,13 @@ _CDT = {torch.bfloat16: "bf16", torch.float16: "fp16", torch.float32: "fp32"}
 
 def fill_expert_outputs(comm, T, device, seed=EO_SEED, special=False, caller=False):
     """Writes the stand-in expert outputs of every rank: into the backend
-    combine-input buffers, or (caller=True) into fresh tensors it returns."""
+    combine-input buffers of the communicator's ranks (all of them, or its
+    partition's), or (caller=True) into fresh tensors of every rank it returns."""
     import workloads
     ep, H = comm.ep_size, comm.hidden
     rows = torch.arange(ep * T, device=device)
     outs = []
-    for d in range(ep):
+    for d in (range(ep) if caller else range(comm.first_rank, comm.first_rank + comm.num_ranks)):
         eo = workloads.expert_output_rows(seed, d, rows, H, device=device, special=special,
                                           dtype=_CDT[comm.combine_dtype])
         if caller:

@@ -29,6 +29,11 @@ def test_bench_line_on_gpu(cuda_device):
     assert "traffic" in rf and (rf["traffic"] is None or rf["traffic"] > 0)
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] == 1 and cb["value"] > 0 and cb["sample"]
+    if len(os.sched_getaffinity(0)) > 1:
+        ca = d["cpu_baseline_all_cores"]
+        assert ca["kind"] == "oracle" and ca["cores"] >= 1 and ca["value"] > 0 and "processes" in ca["sample"]
+    assert rf["peak_kind"] and rf["frac_of_nominal"] == pytest.approx(rf["achieved"] / rf["nominal_peak"])
+    assert d["launch"] == "stream order"
     e2e = d["e2e"]
     assert e2e["value"] > 0 and e2e["h2d_bytes_per_step"] > 0 and e2e["d2h_bytes_per_step"] > 0
     assert "sm_mhz" in d["clocks"] and "reasons" in d["clocks"] and "source" in d["clocks"]
