@@ -216,19 +216,25 @@ def kernel_code_fingerprint() -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(kernel: str, workload: str):
+def recorded_traffic(kernel: str, workload: str, with_source: bool = False):
     """DRAM bytes per launch of `kernel` from the committed ncu summary, when
-    that summary was taken on the current kernel code; else None."""
+    that summary was taken on the current kernel code; else None. With
+    `with_source`, (bytes, how they were obtained) or (None, None)."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
-    if not os.path.exists(path):
-        return None
     src = kernel_code_fingerprint()
-    pat = re.compile(r"^(\S+)\s+workload=(\S+)\s+dram_bytes_per_launch=(\d+)\s+code_sha256=(\S+)")
-    for line in open(path):
-        m = pat.match(line.strip())
-        if m and m.group(1) == kernel and m.group(2) == workload and m.group(4) == src:
-            return int(m.group(3))
-    return None
+    pat = re.compile(r"^(\S+)\s+workload=(\S+)\s+dram_bytes_per_launch=(\d+)\s+code_sha256=(\S+)"
+                     r"(?:\s+scaled_from=T(\d+))?")
+    found = (None, None)
+    if os.path.exists(path):
+        for line in open(path):
+            m = pat.match(line.strip())
+            if m and m.group(1) == kernel and m.group(2) == workload and m.group(4) == src:
+                how = ("ncu capture of a full launch" if m.group(5) is None else
+                       f"ncu capture at {m.group(5)} tokens per rank, scaled to a full launch by the "
+                       "algorithmic bytes (profiles/dram_traffic.txt)")
+                found = (int(m.group(3)), how)
+                break
+    return found if with_source else found[0]
 
 
 class L2Flush:
@@ -662,6 +668,7 @@ def run_ours(args, rank, world):
         "payload_gbs": b["payload"] / (ms / 1e3) / 1e9,
         "roofline": {"bound": "hbm", "kernel": top, "achieved": per[top]["achieved"], "peak": peak,
                      "unit": "GB/s", "frac": per[top]["frac"], "traffic": per[top]["traffic"],
+                     "traffic_source": recorded_traffic(top, wl.name, with_source=True)[1],
                      "peak_source": peak_src,
                      "peak_kind": "a measured copy bandwidth (equal bytes read and written); a kernel whose "
                                   "traffic is mostly reads or mostly writes can stream above it",
