@@ -263,7 +263,8 @@ ep_status ep_dispatch(ep_handle *h, const void *const *hidden, const float *cons
 ep_status ep_dispatch_ex(ep_handle *h, const ep_dispatch_args *args, void *stream,
                          ep_dispatch_result *out);
 
-/* Device pointer to rank `rank`'s backend-owned combine input: [ep_size *
+/* Device pointer to rank `rank`'s backend-owned combine input (a rank the
+ * handle hosts: any rank, unless the handle is a partition): [ep_size *
  * tokens_per_rank, hidden] elements of the handle's combine dtype (bf16
  * unless ep_config.combine_dtype says otherwise) for the pending dispatch. Passing it (or
  * NULL) to ep_combine avoids one copy. Valid between ep_dispatch and
@@ -271,7 +272,11 @@ ep_status ep_dispatch_ex(ep_handle *h, const ep_dispatch_args *args, void *strea
  * NVLinkOneSidedAlltoAll.get_combine_input_buffer). */
 ep_status ep_get_combine_input_buffer(ep_handle *h, int rank, void **out);
 
-/* Combine of the pending dispatch (MoEEpCommunication.combine).
+/* Combine of the pending dispatch (MoEEpCommunication.combine). For a
+ * partition handle: of the source ranks it hosts (output has one entry per
+ * hosted rank), reading every rank's expert outputs (expert_output keeps
+ * ep_size entries; NULL ones are that rank's backend buffer, wherever its
+ * partition's workspace is).
  *  expert_output   NULL = every rank's backend combine input buffer; else
  *                  expert_output[d] is rank d's [ep_size*tokens_per_rank, hidden]
  *                  device buffer of the combine dtype (NULL entry = that rank's

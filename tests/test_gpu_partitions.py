@@ -188,3 +188,28 @@ def test_unconnected_partition_refuses_to_dispatch(cuda_device):
             other.destroy()
     finally:
         c.destroy()
+
+
+def _divisors(n):
+    return [g for g in range(1, n + 1) if n % g == 0]
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_random_partitioned_geometry(cuda_device, seed):
+    """The randomised geometries of the fuzz test, each split into a random
+    number of partitions (a divisor of ep_size), with PDL on half of them."""
+    import random
+
+    from test_gpu_fuzz import _case
+    wl, _ = _case(seed)
+    rng = random.Random(7000 + seed)
+    G = rng.choice(_divisors(wl.ep_size))
+    inp = workloads.make_inputs(wl)
+    comms = _make(wl, G, cuda_device, pdl=rng.random() < 0.5)
+    try:
+        got = _partitioned_round(inp, G, cuda_device, streams=rng.random() < 0.5, comms=comms)
+    finally:
+        for c in comms:
+            c.destroy()
+    disp, out = _oracle(inp)
+    assert_round_equal(inp, got, disp, out)
