@@ -483,11 +483,14 @@ def connect_partitions(comms: Sequence[EpComm]) -> None:
         c.connect(infos)
 
 
-def gather_partition_infos(info: "_lib.EpPartitionInfoC", group=None) -> List["_lib.EpPartitionInfoC"]:
+def gather_partition_infos(info: "_lib.EpPartitionInfoC", group=None,
+                           addresses: Optional[dict] = None) -> List["_lib.EpPartitionInfoC"]:
     """All partitions' descriptions, in partition order, from one process per
     partition of a torch.distributed group: each process passes its own
-    (``EpComm.partition_info()``, its workspace address replaced by one its
-    peers can use). The result is checked with ep_partition_check, so every
+    (``EpComm.partition_info()``). ``addresses`` maps a partition to the
+    device address at which this process reaches that partition's workspace
+    (a peer's memory mapped into this process); it replaces the address the
+    owner reported. The result is checked with ep_partition_check, so every
     process learns of a mismatch in the group's configuration."""
     import torch.distributed as dist
     world = dist.get_world_size(group)
@@ -495,6 +498,9 @@ def gather_partition_infos(info: "_lib.EpPartitionInfoC", group=None) -> List["_
     dist.all_gather_object(gathered, bytes(info), group=group)
     infos = sorted((_lib.EpPartitionInfoC.from_buffer_copy(b) for b in gathered),
                    key=lambda x: x.config.partition)
+    for x in infos:
+        if addresses and x.config.partition in addresses:
+            x.workspace = int(addresses[x.config.partition])
     arr = (_lib.EpPartitionInfoC * len(infos))(*infos)
     check(_lib.load().ep_partition_check(arr, len(infos)))
     return infos
