@@ -912,9 +912,9 @@ ep_status ep_partition_connect(ep_handle *h, const ep_partition_info *infos, int
     ep_status st = ep_partition_check(infos, n);
     if (st != EP_OK)
         return st;
-    const ep_partition_info &me = infos[0].config.num_partitions <= 1 ? infos[0] : infos[h->part];
     if (n != h->num_parts)
         return fail(EP_ERR_INVALID_ARG, "%d descriptions but the handle is one of %d partitions", n, h->num_parts);
+    const ep_partition_info &me = infos[h->part];  // h->part < num_parts == n
     if (me.workspace != h->ws)
         return fail(EP_ERR_INVALID_ARG, "description %d is not of this handle's workspace", h->part);
     if (const char *f = group_config_differs(me.config, h->cfg))

@@ -213,3 +213,32 @@ def test_random_partitioned_geometry(cuda_device, seed):
             c.destroy()
     disp, out = _oracle(inp)
     assert_round_equal(inp, got, disp, out)
+
+
+def test_connect_refuses_another_group(cuda_device):
+    """A handle is connected only with descriptions of its own group: a valid
+    group of another size, or one whose own entry is another workspace, is
+    refused."""
+    wl = CASES["qwen3_mask"]
+    kw = dict(device=cuda_device)
+    four = [EpComm(wl.ep_size, wl.num_experts, wl.top_k, wl.hidden, wl.capacity, num_partitions=4, partition=g, **kw)
+            for g in range(4)]
+    two = [EpComm(wl.ep_size, wl.num_experts, wl.top_k, wl.hidden, wl.capacity, num_partitions=2, partition=g, **kw)
+           for g in range(2)]
+    try:
+        infos2 = [c.partition_info() for c in two]
+        with pytest.raises(EpError, match="one of 4 partitions"):
+            four[3].connect(infos2)
+        swapped = [c.partition_info() for c in four]
+        other = EpComm(wl.ep_size, wl.num_experts, wl.top_k, wl.hidden, wl.capacity, num_partitions=4, partition=1,
+                       **kw)
+        try:
+            swapped[1] = other.partition_info()
+            with pytest.raises(EpError, match="not of this handle's workspace"):
+                four[1].connect(swapped)
+        finally:
+            other.destroy()
+        connect_partitions(four)
+    finally:
+        for c in four + two:
+            c.destroy()
