@@ -23,6 +23,12 @@ columns, K ids, w = 1 when weights are sent:
   combine         P*2H (reads) + 8N (routing state) + N*2H (writes)
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+                    [--pdl] [--partitions NPART]
+
+--partitions NPART runs each round as NPART partitions of the group (ranks in
+NPART contiguous blocks, each with its own workspace and communicator,
+connected with one another): NPART dispatch launches, then NPART combine
+launches per round.
 
 Under torchrun (N > 1) every rank runs an independent replica of the same
 workload on its own GPU (the EP group is simulated inside one GPU, so there
@@ -549,7 +555,7 @@ def workload_config(wl, b, l2_flush):
 # ---------------------------------------------------------------------------
 def run_ours(args, rank, world):
     import torch.distributed as dist
-    from combine_topk_ids_dest_gb300 import EpComm
+    from combine_topk_ids_dest_gb300 import EpComm, connect_partitions
 
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
@@ -557,8 +563,13 @@ def run_ours(args, rank, world):
     inp = workloads.make_inputs(wl)
     b = round_bytes(inp)
     dtype = wl.torch_dtype
-    comm = EpComm(wl.ep_size, wl.num_experts, wl.top_k, wl.hidden, wl.capacity, dtype=dtype,
-                  enable_rank_mask=wl.enable_rank_mask, device=dev, pdl=args.pdl)
+    # one communicator, or (--partitions G) G partitions of the group, each with its own workspace
+    G = args.partitions
+    comms = [EpComm(wl.ep_size, wl.num_experts, wl.top_k, wl.hidden, wl.capacity, dtype=dtype,
+                    enable_rank_mask=wl.enable_rank_mask, device=dev, pdl=args.pdl, num_partitions=G, partition=g)
+             for g in range(G)]
+    if G > 1:
+        connect_partitions(comms)
     mask = inp.active_rank_mask if wl.enable_rank_mask else None
     hid = [x.to(dev) for x in inp.hidden]
     ids = [x.to(dev) for x in inp.topk_ids]
@@ -568,20 +579,23 @@ def run_ours(args, rank, world):
     flush = L2Flush(dev, args.l2_flush)
 
     def dispatch():
-        return comm.dispatch(hid, ids, wts, hidden_states_scale=scl,
-                             runtime_max_tokens_per_rank=wl.runtime_max, active_rank_mask=mask)
+        for c in comms:
+            c.dispatch(_part(hid, c), _part(ids, c), _part(wts, c), hidden_states_scale=_part(scl, c),
+                       runtime_max_tokens_per_rank=wl.runtime_max, active_rank_mask=mask)
 
     def combine():
-        comm.combine(output=out, active_rank_mask=mask)
+        for c in comms:
+            c.combine(output=_part(out, c), active_rank_mask=mask)
 
     # one untimed round to fill the combine-input buffers with expert outputs
-    res = dispatch()
-    rows = torch.arange(wl.ep_size * res.tokens_per_rank, device=dev)
-    for d, buf in enumerate(comm.get_combine_input_buffer()):
-        buf.copy_(workloads.expert_output_rows(1, d, rows, wl.hidden, device=dev))
+    dispatch()
+    rows = torch.arange(wl.ep_size * wl.tokens_per_rank, device=dev)
+    for c in comms:
+        for j, buf in enumerate(c.get_combine_input_buffer()):
+            buf.copy_(workloads.expert_output_rows(1, c.first_rank + j, rows, wl.hidden, device=dev))
     del rows
     combine()
-    launches_per_round = 2 if wl.ep_size * wl.tokens_per_rank > 0 else 0
+    launches_per_round = 2 * G if wl.ep_size * wl.tokens_per_rank > 0 else 0
 
     # The same API calls captured once in CUDA graphs (static shapes):
     # replaying them runs exactly the dispatch and combine kernels, without
@@ -635,11 +649,12 @@ def run_ours(args, rank, world):
 
     # end to end through the public API from pinned host memory
     e2e_steps = max(4, min(args.steps, 20))
-    e2e_ms, h2d_bytes, d2h_bytes = run_e2e(comm, inp, wl, dev, mask, e2e_steps)
+    e2e_ms, h2d_bytes, d2h_bytes = run_e2e(comms, inp, wl, dev, mask, e2e_steps)
     local_cpus = gpu_local_cpus(dev)
 
     total_ms, e2e_ms, eager_ms = reduce_max([total_ms, e2e_ms, eager_ms], device=dev)
-    comm.destroy()
+    for c in comms:
+        c.destroy()
     if rank != 0:
         return
 
@@ -690,6 +705,7 @@ def run_ours(args, rank, world):
         "us_per_round_two_graphs": 1e3 * statistics.mean(t_split),
         "gpu_launches": launches_per_round * args.steps,
         "launch": "programmatic dependent launch (EP_LAUNCH_PDL)" if args.pdl else "stream order",
+        "partitions": G,
         "clocks": clocks.summary(),
     }
     if world == 1 and not args.no_cpu_baseline:
@@ -744,7 +760,12 @@ def gpu_local_cpus(dev):
         return None
 
 
-def run_e2e(comm, inp, wl, dev, mask, steps):
+def _part(lst, c):
+    """The entries of a per-rank list that communicator `c` hosts."""
+    return None if lst is None else lst[c.first_rank:c.first_rank + c.num_ranks]
+
+
+def run_e2e(comms, inp, wl, dev, mask, steps):
     """Rounds through the public API with every step's inputs copied in from
     pinned host memory and its outputs copied back, pipelined over three
     streams with two sets of device buffers: step i's host-to-device copy and
@@ -793,10 +814,13 @@ def run_e2e(comm, inp, wl, dev, mask, steps):
         comp.wait_event(in_ready[k])
         comp.wait_event(out_free[k])
         v = devsets[k][1]
-        comm.dispatch(v["hidden"], v["topk_ids"], v.get("topk_weights"), hidden_states_scale=v.get("scale"),
-                      runtime_max_tokens_per_rank=wl.runtime_max, active_rank_mask=mask)
+        for c in comms:
+            c.dispatch(_part(v["hidden"], c), _part(v["topk_ids"], c), _part(v.get("topk_weights"), c),
+                       hidden_states_scale=_part(v.get("scale"), c), runtime_max_tokens_per_rank=wl.runtime_max,
+                       active_rank_mask=mask)
         in_free[k].record(comp)
-        comm.combine(output=dev_out[k][1], active_rank_mask=mask)
+        for c in comms:
+            c.combine(output=_part(dev_out[k][1], c), active_rank_mask=mask)
         out_ready[k].record(comp)
         with torch.cuda.stream(s_out):
             s_out.wait_event(out_ready[k])
@@ -832,6 +856,8 @@ def main():
                     help="how L2 is evicted between timed steps")
     ap.add_argument("--pdl", action=argparse.BooleanOptionalAction, default=False,
                     help="launch the kernels with programmatic dependent launch")
+    ap.add_argument("--partitions", type=int, default=1,
+                    help="run the group as this many partitions, each with its own workspace")
     ap.add_argument("--tokens-per-rank", type=int, default=None,
                     help="shrink the workload to this many tokens per rank (profiling runs only)")
     args = ap.parse_args()
