@@ -28,7 +28,8 @@ columns, K ids, w = 1 when weights are sent:
 --partitions NPART runs each round as NPART partitions of the group (ranks in
 NPART contiguous blocks, each with its own workspace and communicator,
 connected with one another): NPART dispatch launches, then NPART combine
-launches per round.
+launches per round, one after another, or side by side on a stream each with
+--partition-streams.
 
 Under torchrun (N > 1) every rank runs an independent replica of the same
 workload on its own GPU (the EP group is simulated inside one GPU, so there
@@ -578,14 +579,37 @@ def run_ours(args, rank, world):
     out = [torch.empty(n, wl.hidden, dtype=torch.bfloat16, device=dev) for n in inp.num_tokens]
     flush = L2Flush(dev, args.l2_flush)
 
+    # with --partition-streams each partition's launches go to a stream of its
+    # own, forked from and joined back into the current stream (as a graph
+    # capture sees them), so partitions run side by side as on separate GPUs
+    side = [torch.cuda.Stream(dev) for _ in comms] if args.partition_streams and G > 1 else None
+
+    def each_partition(fn):
+        if side is None:
+            for c in comms:
+                fn(c)
+            return
+        cur = torch.cuda.current_stream(dev)
+        fork = torch.cuda.Event()
+        fork.record(cur)
+        joins = []
+        for c, st in zip(comms, side):
+            st.wait_event(fork)
+            with torch.cuda.stream(st):
+                fn(c)
+                e = torch.cuda.Event()
+                e.record(st)
+                joins.append(e)
+        for e in joins:
+            cur.wait_event(e)
+
     def dispatch():
-        for c in comms:
-            c.dispatch(_part(hid, c), _part(ids, c), _part(wts, c), hidden_states_scale=_part(scl, c),
-                       runtime_max_tokens_per_rank=wl.runtime_max, active_rank_mask=mask)
+        each_partition(lambda c: c.dispatch(_part(hid, c), _part(ids, c), _part(wts, c),
+                                            hidden_states_scale=_part(scl, c),
+                                            runtime_max_tokens_per_rank=wl.runtime_max, active_rank_mask=mask))
 
     def combine():
-        for c in comms:
-            c.combine(output=_part(out, c), active_rank_mask=mask)
+        each_partition(lambda c: c.combine(output=_part(out, c), active_rank_mask=mask))
 
     # one untimed round to fill the combine-input buffers with expert outputs
     dispatch()
@@ -705,7 +729,7 @@ def run_ours(args, rank, world):
         "us_per_round_two_graphs": 1e3 * statistics.mean(t_split),
         "gpu_launches": launches_per_round * args.steps,
         "launch": "programmatic dependent launch (EP_LAUNCH_PDL)" if args.pdl else "stream order",
-        "partitions": G,
+        "partitions": G, "partition_streams": side is not None,
         "clocks": clocks.summary(),
     }
     if world == 1 and not args.no_cpu_baseline:
@@ -858,6 +882,8 @@ def main():
                     help="launch the kernels with programmatic dependent launch")
     ap.add_argument("--partitions", type=int, default=1,
                     help="run the group as this many partitions, each with its own workspace")
+    ap.add_argument("--partition-streams", action="store_true",
+                    help="launch each partition on a stream of its own (side by side)")
     ap.add_argument("--tokens-per-rank", type=int, default=None,
                     help="shrink the workload to this many tokens per rank (profiling runs only)")
     args = ap.parse_args()
