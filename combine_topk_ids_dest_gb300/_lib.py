@@ -44,7 +44,7 @@ EXPORTS = ("ep_is_supported", "ep_workspace_size", "ep_create", "ep_create_with_
            "ep_dispatch", "ep_get_combine_input_buffer", "ep_combine", "ep_destroy",
            "ep_rank_mask", "ep_last_error", "ep_combine_noalloc", "ep_workspace_size_ex",
            "ep_create_ex", "ep_dispatch_ex", "ep_binary_version", "ep_partition_describe",
-           "ep_partition_check", "ep_partition_connect")
+           "ep_partition_check", "ep_partition_connect", "ep_partition_info_of")
 EP_NOALLOC_MAX_SLOTS = 65536
 
 
@@ -154,6 +154,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         L.ep_binary_version.restype = i32
         L.ep_partition_describe.argtypes = [ctypes.POINTER(EpConfigC), P, sz, ctypes.POINTER(EpPartitionInfoC)]
         L.ep_partition_describe.restype = i32
+        L.ep_partition_info_of.argtypes = [P, ctypes.POINTER(EpPartitionInfoC)]
+        L.ep_partition_info_of.restype = i32
         L.ep_partition_check.argtypes = [ctypes.POINTER(EpPartitionInfoC), i32]
         L.ep_partition_check.restype = i32
         L.ep_partition_connect.argtypes = [P, ctypes.POINTER(EpPartitionInfoC), i32]

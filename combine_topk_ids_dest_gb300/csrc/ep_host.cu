@@ -839,6 +839,13 @@ ep_status ep_partition_describe(const ep_config *cfg, void *workspace, size_t by
     return ok();
 }
 
+ep_status ep_partition_info_of(const ep_handle *h, ep_partition_info *out)
+{
+    if (!h)
+        return fail(EP_ERR_INVALID_ARG, "handle is NULL");
+    return ep_partition_describe(&h->cfg, h->ws, h->ws_bytes, out);
+}
+
 namespace {
 
 // Name of the first field in which two configurations of one group differ

@@ -367,6 +367,10 @@ typedef struct {
  * no GPU. EP_ERR_INVALID_ARG on a bad configuration. */
 ep_status ep_partition_describe(const ep_config *cfg, void *workspace, size_t bytes, ep_partition_info *out);
 
+/* ep_partition_describe of a handle: its configuration and its workspace
+ * (also one the library allocated). Host only. */
+ep_status ep_partition_info_of(const ep_handle *h, ep_partition_info *out);
+
 /* Checks that infos[0..n) describe one partitioned group: n ==
  * num_partitions, infos[p] is partition p, all configurations equal but for
  * `partition`, each layout is the one its configuration gives, workspaces

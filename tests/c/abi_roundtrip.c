@@ -8,7 +8,8 @@
  * {2,3}. Checks every receive id row, the routed hidden rows, and three
  * combine outputs worked by hand; then a second round through
  * ep_dispatch_ex with device-side token counts (rank 0 sends only its first
- * token). Exit status 0 on success.
+ * token); then the first round again as a partitioned group of two
+ * partitions. Exit status 0 on success.
  */
 #include <stdint.h>
 #include <stdio.h>
@@ -176,6 +177,68 @@ int main(void)
     cudaFree(d_counts);
     if (!ok(ep_destroy(h), "ep_destroy"))
         return 1;
+
+    /* The same example as a partitioned group: two partitions of one rank
+     * each, every partition with a handle and a workspace of its own. Each
+     * dispatch writes its rank's tokens into both ranks' receive rows; each
+     * combine reads both ranks' combine inputs. */
+    ep_config cfg;
+    memset(&cfg, 0, sizeof cfg);
+    cfg.ep_size = EP;
+    cfg.num_experts = 4;
+    cfg.top_k = 2;
+    cfg.hidden = H;
+    cfg.max_tokens_per_rank = T;
+    cfg.dtype = EP_DTYPE_BF16;
+    cfg.scale_cols = EP_SCALE_COLS_DEFAULT;
+    cfg.combine_dtype = EP_DTYPE_BF16;
+    cfg.num_partitions = EP;
+    ep_handle *part[EP];
+    ep_partition_info info[EP];
+    for (int g = 0; g < EP; ++g) {
+        cfg.partition = g;
+        if (!ok(ep_create_ex(&cfg, NULL, 0, &part[g]), "ep_create_ex (partition)") ||
+            !ok(ep_partition_info_of(part[g], &info[g]), "ep_partition_info_of"))
+            return 1;
+        expect(info[g].first_rank == g && info[g].num_ranks == 1, "one rank per partition");
+    }
+    expect(ep_dispatch(part[0], hidden, NULL, ids, NULL, counts, -1, UINT64_MAX, NULL, &res) == EP_ERR_STATE,
+           "an unconnected partition refuses to dispatch");
+    for (int g = 0; g < EP; ++g)
+        if (!ok(ep_partition_connect(part[g], info, EP), "ep_partition_connect"))
+            return 1;
+    ep_dispatch_result pres[EP];
+    for (int g = 0; g < EP; ++g)
+        if (!ok(ep_dispatch(part[g], &hidden[g], NULL, &ids[g], NULL, &counts[g], -1, UINT64_MAX, NULL, &pres[g]),
+                "ep_dispatch (partition)"))
+            return 1;
+    for (int g = 0; g < EP; ++g) {
+        int32_t got[EP * T][2];
+        expect(pres[g].first_rank == g && pres[g].num_ranks == 1, "partition result geometry");
+        cudaMemcpy(got, pres[g].recv_topk_ids[0], sizeof got, cudaMemcpyDeviceToHost);
+        expect(memcmp(got, want[g], sizeof got) == 0, "partition id plane");
+        void *buf;
+        if (!ok(ep_get_combine_input_buffer(part[g], g, &buf), "ep_get_combine_input_buffer (partition)"))
+            return 1;
+        cudaMemcpy(buf, eo[g], sizeof eo[g], cudaMemcpyHostToDevice);
+    }
+    cudaMemcpy(row, (const char *)pres[1].recv_hidden[0] + 3 * H * 2, sizeof row, cudaMemcpyDeviceToHost);
+    expect(memcmp(row, h1, sizeof row) == 0, "partition 1 receives token 0 of rank 1");
+    cudaMemcpy(row, (const char *)pres[1].recv_hidden[0] + 1 * H * 2, sizeof row, cudaMemcpyDeviceToHost);
+    expect(memcmp(row, h0 + H, sizeof row) == 0, "partition 1 receives token 1 of rank 0 from partition 0");
+    for (int g = 0; g < EP; ++g)
+        if (!ok(ep_combine(part[g], NULL, &out[g], UINT64_MAX, NULL), "ep_combine (partition)"))
+            return 1;
+    cudaMemcpy(o0, d_o0, sizeof o0, cudaMemcpyDeviceToHost);
+    cudaMemcpy(o1, d_o1, sizeof o1, cudaMemcpyDeviceToHost);
+    for (int c = 0; c < H; ++c) {
+        expect(o0[0][c] == 0x4000, "partitions: token (0,0) = 2.0");
+        expect(o0[1][c] == 0x3F80, "partitions: token (0,1) sums ranks 0 and 1 across partitions");
+        expect(o1[0][c] == 0x3FC0, "partitions: token (1,0) = 1.5");
+    }
+    for (int g = 0; g < EP; ++g)
+        if (!ok(ep_destroy(part[g]), "ep_destroy (partition)"))
+            return 1;
     if (failures)
         return 1;
     printf("abi_roundtrip: ok\n");
