@@ -240,7 +240,9 @@ class EpComm:
                  num_tokens: Optional[Sequence[int]] = None) -> EpDispatchResult:
         """Scatter each rank's tokens to the ranks holding one of their top-k experts.
 
-        Per rank s: ``hidden_states[s]`` [n_s, hidden] (dtype of the
+        Per rank s (of the communicator's ranks: all ``ep_size`` of them, or
+        a partition's ``num_ranks``, entry j being rank ``first_rank + j``):
+        ``hidden_states[s]`` [n_s, hidden] (dtype of the
         communicator), ``topk_ids[s]`` int32 [n_s, top_k], optional
         ``topk_weights[s]`` fp32 [n_s, top_k] and ``hidden_states_scale[s]``
         fp32 [n_s, scale_cols]. Weights and scales are all-or-none over ranks.
