@@ -149,6 +149,7 @@ class EpComm:
         self._stacked = False
         self._dev_index = self.device.index if self.device.index is not None else torch.cuda.current_device()
         self._views = {}  # (kind, T) -> per-rank views of the workspace
+        self._peer_ws = None  # peers' workspaces mapped into this process (connect_across_processes)
 
     # -- MoEEpCommunication.is_platform_supported ---------------------------
     @classmethod
@@ -201,6 +202,30 @@ class EpComm:
         self._live()
         arr = (_lib.EpPartitionInfoC * len(infos))(*infos)
         check(self._L.ep_partition_connect(self._h, arr, len(infos)))
+
+    def connect_across_processes(self, group=None) -> None:
+        """Connect with every partition of the group when each partition lives
+        in a process of its own (one per partition, on this GPU or on GPUs that
+        can map each other's memory) of a torch.distributed ``group``: the
+        workspaces are shared as CUDA IPC handles (the way torch.multiprocessing
+        shares CUDA tensors), every peer's is mapped into this process, and the
+        descriptions are gathered and checked (gather_partition_infos). The
+        mapped peer workspaces are held until destroy(); every process must keep
+        its communicator alive until all of them are done with it (e.g. a
+        barrier before destroy())."""
+        import pickle
+        from multiprocessing.reduction import ForkingPickler
+
+        import torch.distributed as dist
+        self._live()
+        world = dist.get_world_size(group)
+        mine = (self.partition, bytes(ForkingPickler.dumps(self._ws)))
+        gathered = [None] * world
+        dist.all_gather_object(gathered, mine, group=group)
+        self._peer_ws = {p: pickle.loads(b) for p, b in gathered if p != self.partition}
+        infos = gather_partition_infos(self.partition_info(), group,
+                                       addresses={p: t.data_ptr() for p, t in self._peer_ws.items()})
+        self.connect(infos)
 
     def _check_stacked(self, name, t, M, cols, dtype):
         """Checks one stacked operand, [num_ranks, M, cols] (M from the tensor when
@@ -464,6 +489,7 @@ class EpComm:
         self._h = None
         self._views = {}
         self._ws = None
+        self._peer_ws = None
 
     def __del__(self):
         try:

@@ -1,10 +1,11 @@
 """A partitioned group with one process per partition, all on one GPU.
 
-Each process creates its partition, hands its workspace to the others as a
-CUDA tensor through torch.multiprocessing (the memory is mapped into each
-receiving process), exchanges its description over a gloo group
-(gather_partition_infos, with the peers' workspaces at the addresses mapped
-here) and connects. Each process then dispatches its own ranks' tokens
+Each process creates its partition and connects with the others over a gloo
+group: either with EpComm.connect_across_processes (workspaces shared as CUDA
+IPC handles inside the gathered objects) or by hand, handing its workspace to
+the others as a CUDA tensor through torch.multiprocessing queues (the memory
+is mapped into each receiving process) and then gather_partition_infos with
+the peers' workspaces at the addresses mapped here. Each process then dispatches its own ranks' tokens
 straight into the other processes' receive buffers, writes its ranks' stand-in
 expert outputs, and combines its own tokens from every process's buffers.
 The phases are ordered on the host (stream synchronisation, then a gloo
@@ -31,7 +32,7 @@ def _free_port():
         return s.getsockname()[1]
 
 
-def _child(rank, world, port, queues, results):
+def _child(rank, world, port, queues, results, by_hand):
     import numpy as np
     import torch.distributed as dist
 
@@ -49,13 +50,16 @@ def _child(rank, world, port, queues, results):
         inp = workloads.make_inputs(wl)
         comm = EpComm(wl.ep_size, wl.num_experts, wl.top_k, wl.hidden, wl.capacity, dtype=wl.torch_dtype,
                       enable_rank_mask=True, device=dev, num_partitions=world, partition=rank)
-        for h in range(world):  # this partition's workspace, mapped into every other process
-            if h != rank:
-                queues[h].put((rank, comm._ws))
-        peers = dict(queues[rank].get(timeout=120) for _ in range(world - 1))
-        infos = gather_partition_infos(comm.partition_info(),
-                                       addresses={h: t.data_ptr() for h, t in peers.items()})
-        comm.connect(infos)
+        if by_hand:
+            for h in range(world):  # this partition's workspace, mapped into every other process
+                if h != rank:
+                    queues[h].put((rank, comm._ws))
+            peers = dict(queues[rank].get(timeout=120) for _ in range(world - 1))
+            infos = gather_partition_infos(comm.partition_info(),
+                                           addresses={h: t.data_ptr() for h, t in peers.items()})
+            comm.connect(infos)
+        else:
+            comm.connect_across_processes()
         lo, hi = comm.first_rank, comm.first_rank + comm.num_ranks
         mask = inp.active_rank_mask
         res = comm.dispatch([x.to(dev) for x in inp.hidden[lo:hi]], [x.to(dev) for x in inp.topk_ids[lo:hi]],
@@ -102,14 +106,14 @@ def _child(rank, world, port, queues, results):
         dist.destroy_process_group()
 
 
-@pytest.mark.parametrize("world", [2, 4])
-def test_one_process_per_partition(cuda_device, world):
+@pytest.mark.parametrize("world,by_hand", [(2, True), (4, True), (2, False), (4, False)])
+def test_one_process_per_partition(cuda_device, world, by_hand):
     import torch.multiprocessing as mp
     ctx = mp.get_context("spawn")
     queues = [ctx.Queue() for _ in range(world)]
     results = ctx.Queue()
     port = _free_port()
-    procs = [ctx.Process(target=_child, args=(r, world, port, queues, results)) for r in range(world)]
+    procs = [ctx.Process(target=_child, args=(r, world, port, queues, results, by_hand)) for r in range(world)]
     for p in procs:
         p.start()
     try:
