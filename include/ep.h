@@ -348,7 +348,10 @@ ep_status ep_binary_version(int *version);
  * runtime_max_tokens_per_rank and mask; a partition's receive buffers are
  * complete once every partition's dispatch has completed, and a combine may
  * start only after every rank's expert outputs are written: ordering across
- * partitions is the caller's (stream order, or events between streams). */
+ * partitions is the caller's (stream order, or events between streams).
+ * A connected handle keeps its peers' addresses: a partition's workspace must
+ * stay allocated while any handle of the group may still dispatch or combine,
+ * so destroy a group's handles together, after their last work has run. */
 
 /* One partition as its peers see it. */
 typedef struct {
