@@ -28,6 +28,15 @@
 //   are stored as they are) (page "flashinfer.moe_ep.MoEEpCommunication",
 //   combine(): per token, the ranks' expert outputs are added up).
 //
+// A launch handles a range of source ranks (all of them, or one partition's
+// of a partitioned group) and reaches every destination rank's buffers
+// through per-rank address tables, advanced on the host to the range's first
+// row so that the launch's own slot index addresses them; where each rank's
+// buffers live (one workspace or several) does not matter to the kernels.
+// Both kernels open with griddepcontrol.launch_dependents / .wait, which let
+// a programmatically dependent launch (EP_LAUNCH_PDL) be scheduled early and
+// are no-ops otherwise.
+//
 // With device-side token counts the dispatch reads each rank's count when it
 // runs (clamped to the host maximum) and leaves it for the combine, whose
 // blocks past it exit. In the checked build (EP_CHECKED) every global access
