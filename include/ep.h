@@ -376,7 +376,8 @@ ep_status ep_partition_info_of(const ep_handle *h, ep_partition_info *out);
 
 /* Checks that infos[0..n) describe one partitioned group: n ==
  * num_partitions, infos[p] is partition p, all configurations equal but for
- * `partition`, each layout is the one its configuration gives, workspaces
+ * `partition` and `launch_flags` (a local choice), each layout is the one
+ * its configuration gives, workspaces
  * are large enough, 256-byte aligned and do not overlap. Host only;
  * EP_ERR_INVALID_ARG with the first problem in ep_last_error otherwise. */
 ep_status ep_partition_check(const ep_partition_info *infos, int n);
