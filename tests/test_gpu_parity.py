@@ -115,3 +115,56 @@ def test_rounds_reuse_handle_with_changing_T(cuda_device):
             assert_round_equal(inp, got, disp, out)
     finally:
         comm.destroy()
+
+
+def test_packed_fp4_payload_with_byte_scales(cuda_device):
+    """A quantised payload of any byte-aligned format travels as opaque bytes
+    (MoEEpCommunication.dispatch: hidden_states "unquantized or quantized",
+    [local_num_tokens, *]): here packed 4-bit values (two per byte, 7168 values
+    = 3584 bytes per row, passed as an 8-bit payload) with one 8-bit scale per
+    16 values (448 bytes per row, passed as 112 fp32 words). Scale bytes stay
+    below 0x7F, so no 32-bit word is a NaN. Receive rows must equal the
+    source bytes exactly, and the ids and weights the oracle's."""
+    import torch
+
+    import oracle
+    from combine_topk_ids_dest_gb300 import EpComm
+    from ep_testutil import INV, raw_bytes, to_dev
+    values, group = 7168, 16
+    row_bytes, scale_bytes = values // 2, values // group
+    wl = workloads.EpWorkload(name="fp4_bytes", ep_size=8, num_experts=64, top_k=8, hidden=row_bytes,
+                              dtype="fp8_e4m3", capacity=24, runtime_max=None, counts=("uniform", 0, 24),
+                              dropped_ranks=(6,), seed=81)
+    inp = workloads.make_inputs(wl)
+    g = torch.Generator().manual_seed(82)
+    rows = [torch.randint(0, 256, (n, row_bytes), generator=g, dtype=torch.uint8) for n in inp.num_tokens]
+    scales = [torch.randint(0, 0x7F, (n, scale_bytes), generator=g, dtype=torch.uint8) for n in inp.num_tokens]
+    hid = [r.view(torch.float8_e4m3fn) for r in rows]
+    scl = [s.view(torch.float32) for s in scales]  # [n, 112] words of 4 scale bytes
+    comm = EpComm(wl.ep_size, wl.num_experts, wl.top_k, row_bytes, wl.capacity, dtype=torch.float8_e4m3fn,
+                  enable_rank_mask=True, device=cuda_device, scale_cols=scale_bytes // 4)
+    try:
+        mask = inp.active_rank_mask
+        res = comm.dispatch(to_dev(hid, cuda_device), to_dev(inp.topk_ids, cuda_device),
+                            to_dev(inp.topk_weights, cuda_device), hidden_states_scale=to_dev(scl, cuda_device),
+                            active_rank_mask=mask)
+        T = res.tokens_per_rank
+        want = oracle.dispatch(wl.ep_size, wl.num_experts, wl.top_k, T, inp.num_tokens, rows, inp.topk_ids,
+                               scale=[s.view(torch.float32) for s in scales], topk_weights=inp.topk_weights,
+                               mask_enabled=True, active_rank_mask=mask, row_bytes=row_bytes,
+                               scale_cols=scale_bytes // 4)
+        rows_id = torch.arange(wl.ep_size * T, device=cuda_device)
+        for d, buf in enumerate(comm.get_combine_input_buffer()):
+            buf.copy_(workloads.expert_output_rows(5, d, rows_id, row_bytes, device=cuda_device))
+        comm.combine(active_rank_mask=mask)
+        torch.cuda.synchronize(cuda_device)
+        for d in range(wl.ep_size):
+            np.testing.assert_array_equal(res.topk_ids[d].cpu().numpy(), want.recv_ids[d])
+            valid = (want.recv_ids[d] != INV).any(axis=1)
+            np.testing.assert_array_equal(raw_bytes(res.hidden_states[d].cpu())[valid], want.recv_hidden[d][valid])
+            np.testing.assert_array_equal(res.hidden_states_scale[d].cpu().numpy()[valid].view(np.uint32),
+                                          want.recv_scale[d][valid].view(np.uint32))
+            np.testing.assert_array_equal(res.topk_weights[d].cpu().numpy()[valid].view(np.uint32),
+                                          want.recv_weights[d][valid].view(np.uint32))
+    finally:
+        comm.destroy()
