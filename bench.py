@@ -506,7 +506,7 @@ def run_reference(args, rank, world):
     """The oracle timed as the reference arm (rank 0 only)."""
     if rank != 0:
         return
-    wl = workloads.WORKLOADS[args.workload]
+    wl = workloads.by_name(args.workload)
     inp = workloads.make_inputs(wl)
     full = round_bytes(inp)
     # the whole arm takes about --reference-seconds for any step count (the
@@ -560,7 +560,7 @@ def run_ours(args, rank, world):
 
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
-    wl = workloads.WORKLOADS[args.workload]
+    wl = workloads.by_name(args.workload)
     inp = workloads.make_inputs(wl)
     b = round_bytes(inp)
     dtype = wl.torch_dtype
@@ -870,7 +870,8 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="dsv3_prefill", choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--workload", default="dsv3_prefill",
+                    choices=sorted(workloads.WORKLOADS) + sorted(workloads.GEOMETRIES))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle sample size, in seconds")
     ap.add_argument("--reference-seconds", type=float, default=120.0,
@@ -891,7 +892,7 @@ def main():
         ap.error("--warmup must be at least 3")
 
     if args.tokens_per_rank is not None:
-        wl = workloads.WORKLOADS[args.workload]
+        wl = workloads.by_name(args.workload)
         m = args.tokens_per_rank
         counts = wl.counts
         if counts[0] == "uniform":

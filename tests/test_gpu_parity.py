@@ -36,6 +36,12 @@ def test_shrunk_workloads(cuda_device, name, hidden):
     _check(small(workloads.WORKLOADS[name], hidden=hidden, tokens=40), cuda_device)
 
 
+@pytest.mark.parametrize("name", sorted(workloads.GEOMETRIES))
+def test_shrunk_geometries(cuda_device, name):
+    # the further bandwidth geometries (ep 8..64, top_k 4..32, bf16/fp8) at oracle-friendly sizes
+    _check(small(workloads.GEOMETRIES[name], hidden=512, tokens=12), cuda_device)
+
+
 def test_mixtral_full_hidden_small_tokens(cuda_device):
     _check(small(workloads.WORKLOADS["mixtral_decode"], hidden=4096, tokens=20), cuda_device)
 

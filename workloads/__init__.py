@@ -111,6 +111,31 @@ WORKLOADS = {
 }
 
 
+# Further EP geometries, for the bandwidth across ep_size, top_k, payload type
+# and row width (bench.py --workload <name>); they are not among the five
+# configurations above. Every rank sends a full capacity of tokens.
+GEOMETRIES = {
+    name: EpWorkload(name=name, runtime_max=None, counts=("full",), **kw)
+    for name, kw in {
+        "geom_ep8_fp8": dict(ep_size=8, num_experts=64, top_k=8, hidden=7168, dtype="fp8_e4m3", scales=True,
+                             capacity=2048),
+        "geom_ep16_fp8": dict(ep_size=16, num_experts=128, top_k=8, hidden=7168, dtype="fp8_e4m3", scales=True,
+                              capacity=1024),
+        "geom_ep64_fp8": dict(ep_size=64, num_experts=256, top_k=8, hidden=7168, dtype="fp8_e4m3", scales=True,
+                              capacity=512),
+        "geom_ep32_bf16_k4": dict(ep_size=32, num_experts=256, top_k=4, hidden=7168, dtype="bf16", capacity=512),
+        "geom_ep32_bf16_k16": dict(ep_size=32, num_experts=256, top_k=16, hidden=4096, dtype="bf16", capacity=512),
+        "geom_ep64_bf16_k32": dict(ep_size=64, num_experts=64, top_k=32, hidden=2048, dtype="bf16", capacity=128,
+                                   ids="uniform_dups"),
+    }.items()
+}
+
+
+def by_name(name: str) -> EpWorkload:
+    """One of the five workloads, or one of the further geometries."""
+    return WORKLOADS[name] if name in WORKLOADS else GEOMETRIES[name]
+
+
 @dataclass
 class EpInputs:
     """Per-source-rank host tensors of one workload (all on the CPU)."""
